@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Benchmark of the skinny decode projection on one GB300 (or N replicas).
+
+Metric: weight-stream GB/s (and us per projection) against the HBM roofline,
+at decode batch M = 1..64.  One step = one pass of the whole hot path over
+one batch of synthetic inputs:
+
+  sweep (default)  the batch sweep M in {1,2,4,8,16,32,64}, K = N = 7168,
+                   bf16, no residual: 7 projections, each with its own
+                   102.8 MB weight (seed = index of M), so a step streams
+                   719 MB of weights and no weight is L2-resident when its
+                   projection runs (inputs larger than the 126 MB L2).
+  chain            the five projections of a decode layer at M = 1, 8, 64,
+                   the next weight prefetched into L2 on a side stream.
+  wide / deepk     the wide input projection and the deep-K output projection
+                   with residual, at their M values.
+
+`value` is the whole job's weight bytes / device time (CUDA events around the
+timed steps, max over ranks).  `e2e` repeats the measurement through the
+public API with the step's activations copied from pinned host memory and its
+outputs copied back inside the timed region (weights stay resident: they are
+parameters, not per-step inputs).  `--impl reference` times the CPU oracle on
+the same metric instead (a bounded sample of each step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "weight-stream GB/s and µs/projection vs GB300 HBM roofline at M=1..64"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ workloads
+def workload(name: str):
+    from projection_gemm_gb300 import inputs as I
+    if name == "sweep":
+        projs = [I.sweep(m) for m in I.SWEEP_M]
+        desc = ("batch sweep M in {1,2,4,8,16,32,64}, K=N=7168, bf16 W~N(0,1/K), x~N(0,1), "
+                "no residual, seed = index of M")
+        return projs, desc, {"M": list(I.SWEEP_M), "N": 7168, "K": 7168, "epilogue": "bf16"}
+    if name == "wide":
+        return ([I.wide(m) for m in I.WIDE_M], "wide input projection M in {1,2,8,32,64}, K=7168, N=12288, "
+                "1% of W rows x16", {"M": list(I.WIDE_M), "N": 12288, "K": 7168, "epilogue": "bf16"})
+    if name == "deepk":
+        return ([I.deepk(m) for m in I.DEEPK_M], "deep-K output projection + residual M in {1,4,16,64}, "
+                "K=16384, N=7168, residual~N(0,4)", {"M": list(I.DEEPK_M), "N": 7168, "K": 16384,
+                                                     "epilogue": "bf16_residual"})
+    if name == "chain":
+        projs = [p for m in I.CHAIN_M for p in I.chain(m)]
+        return projs, ("decode-layer chain at M in {1,8,64}: 7168->12288, 8192->7168 (+res), "
+                       "7168->384 (fp32), 7168->4096, 4096->7168 (+res); next W prefetched to L2 "
+                       "on a side stream"), {"M": list(I.CHAIN_M), "stages": [list(s) for s in I.CHAIN_STAGES]}
+    if name == "pr1":
+        return [I.pr1()], "PR1: M=1, K=N=1024, + residual", {"M": [1], "N": 1024, "K": 1024,
+                                                              "epilogue": "bf16_residual"}
+    raise ValueError(name)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# --------------------------------------------------------------- clock probe
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [s for t, s in self.samples if self.t0 is not None and self.t0 - 0.1 <= t <= self.t1 + 0.25]
+        if not rows and self.samples:
+            rows = [self.samples[-1][1]]
+        sm, mx, reasons, power = [], None, set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------ distributed
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(elapsed_s: float, units: float, world: int):
+    """Max of the elapsed time and sum of the units over all ranks."""
+    if world == 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------- CPU oracle
+class OracleSample:
+    """The oracle over the first R W rows of every projection of one step, R
+    calibrated once for about `seconds` of CPU work (the oracle as it stands,
+    all host cores through its OpenMP loop)."""
+
+    def __init__(self, data, seconds: float):
+        import oracle.oracle as O
+        self.O = O
+        self.data = data            # [(Projection, x bits, W bits, residual bits or None)]
+        b, dt = self.run_rows(16)
+        nmax = max(p.N for p, *_ in data)
+        self.rows = max(16, min(nmax, int(16 * seconds / max(dt, 1e-6))))
+        self.cores = O.max_threads()
+        self.desc = (f"oracle (fp64, {self.cores} threads) on the first {self.rows} W rows of each of the "
+                     f"step's {len(data)} projections, every M")
+
+    def run_rows(self, rows):
+        import numpy as np
+        wbytes = 0
+        t0 = time.perf_counter()
+        for p, xb, wb, rb in self.data:
+            r = min(rows, p.N)
+            self.O.linear(xb, np.ascontiguousarray(wb[:r]),
+                          None if rb is None else np.ascontiguousarray(rb[:, :r]))
+            wbytes += 2 * r * p.K
+        return wbytes, time.perf_counter() - t0
+
+    def run(self):
+        b, dt = self.run_rows(self.rows)
+        return b / dt / 1e9, dt
+
+
+def host_data(projs):
+    from projection_gemm_gb300.inputs import bits, generate
+    out = []
+    for p in projs:
+        t = generate(p)
+        out.append((p, bits(t.x), bits(t.W), None if t.res is None else bits(t.res)))
+    return out
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    from projection_gemm_gb300 import build as B
+    from projection_gemm_gb300 import skg
+    from projection_gemm_gb300.inputs import generate
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    B.build()
+    skg.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    projs, desc, cfg = workload(args.workload)
+    peak_hbm, peak_tf, peak_src = load_peaks()
+
+    # operands resident in HBM
+    ops, hostcopy = [], []
+    for p in projs:
+        t = generate(p)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            from projection_gemm_gb300.inputs import bits
+            hostcopy.append((p, bits(t.x), bits(t.W), None if t.res is None else bits(t.res)))
+        plan = skg.Plan(p.M, p.N, p.K, p.epilogue)
+        plan.set_pdl(bool(args.pdl))
+        dt = torch.float32 if p.epilogue == "fp32" else torch.bfloat16
+        ops.append(dict(p=p, plan=plan, info=plan.info(),
+                        x=t.x.to(dev), W=t.W.to(dev),
+                        res=None if t.res is None else t.res.to(dev),
+                        y=torch.empty(p.M, p.N, dtype=dt, device=dev),
+                        hx=t.x.pin_memory(), hres=None if t.res is None else t.res.pin_memory(),
+                        hy=torch.empty(p.M, p.N, dtype=dt).pin_memory()))
+        del t
+    chain = args.workload == "chain"
+    side = torch.cuda.Stream(device=dev)
+    stream = torch.cuda.current_stream(dev)
+    if chain and args.prefetch is not None:
+        for o in ops:
+            skg.skg_plan_set_prefetch_fraction(o["plan"].handle, args.prefetch)
+
+    def step(events=None):
+        for i, o in enumerate(ops):
+            if chain and i + 1 < len(ops) and ops[i + 1]["info"]["prefetch_bytes"] > 0:
+                side.wait_stream(stream)
+                ops[i + 1]["plan"].prefetch(ops[i + 1]["W"], side)
+            if events is not None:
+                events[i].record(stream)
+            o["plan"].run(o["x"], o["W"], o["res"], o["y"], stream)
+            if chain and i + 1 < len(ops):
+                stream.wait_stream(side)
+        if events is not None:
+            events[len(ops)].record(stream)
+
+    launches_per_step = len(ops) + (sum(1 for o in ops[1:] if o["info"]["prefetch_bytes"] > 0) if chain else 0)
+    wbytes_step = sum(o["p"].weight_bytes() for o in ops)
+
+    warm = max(3, args.warmup)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(warm):
+        step()
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / warm
+    K = args.steps if args.steps else max(20, min(40000, int(args.seconds / max(est, 1e-6))))
+    sample_every = max(1, K // 300)
+    sampled = list(range(0, K, sample_every))
+    evs = {k: [torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for k in sampled}
+
+    clocks = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.6)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    start.record(stream)
+    for k in range(K):
+        step(evs.get(k))
+    end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if world > 1:
+        dist.barrier()
+    if clocks:
+        time.sleep(0.3)
+        clocks.stop()
+        clocks.window(w0, w1)
+    elapsed = start.elapsed_time(end) / 1e3
+    max_t, total_bytes = aggregate(elapsed, wbytes_step * K, world)
+    value = total_bytes / max_t / 1e9
+
+    # per-launch durations from the sampled steps (events on the launch stream)
+    per = {i: [] for i in range(len(ops))}
+    for k in sampled:
+        e = evs[k]
+        for i in range(len(ops)):
+            per[i].append(e[i].elapsed_time(e[i + 1]) * 1e3)  # us
+    per_m, kern = {}, {}
+    for i, o in enumerate(ops):
+        p = o["p"]
+        us = statistics.median(per[i])
+        t_ideal = max(p.algorithmic_bytes() / (peak_hbm * 1e9), p.flops() / (peak_tf * 1e12)) * 1e6
+        key = f"{p.name}"
+        per_m[key] = {"M": p.M, "N": p.N, "K": p.K, "kernel": o["info"]["kernel"], "split": o["info"]["split_k"],
+                      "us": round(us, 3), "weight_gbs": round(p.weight_bytes() / us / 1e3, 1),
+                      "roofline_frac": round(t_ideal / us, 4)}
+        kk = kern.setdefault(o["info"]["kernel"], {"bytes": 0.0, "us": 0.0, "launches": 0})
+        kk["bytes"] += p.algorithmic_bytes() * len(per[i])
+        kk["us"] += sum(per[i])
+        kk["launches"] += len(per[i])
+    dom = max(kern, key=lambda k: kern[k]["us"])
+    achieved = kern[dom]["bytes"] / (kern[dom]["us"] * 1e-6) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", f"traffic_{dom}_{args.workload}.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak_hbm, "unit": "GB/s",
+                "frac": round(achieved / peak_hbm, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
+                "launches_timed": kern[dom]["launches"]}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": warm, "ms_per_step": round(max_t / K * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": desc, **cfg, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": ("inputs larger than L2: every step streams %.1f MB of distinct weights" % (wbytes_step / 1e6)),
+                   "pdl": bool(args.pdl)},
+        "per_projection": per_m, "roofline": roofline,
+        "gpu_launches": launches_per_step * K,
+    }
+    if clocks:
+        result["clocks"] = clocks.summary()
+
+    # e2e: activations from pinned host memory, outputs back, every step
+    if not args.no_e2e:
+        Ke = max(3, min(K, int(args.e2e_seconds / max(est, 1e-6))))
+        h2d = sum(o["hx"].numel() * 2 + (o["hres"].numel() * 2 if o["hres"] is not None else 0) for o in ops)
+        d2h = sum(o["hy"].numel() * o["hy"].element_size() for o in ops)
+
+        def e2e_step():
+            for i, o in enumerate(ops):
+                o["x"].copy_(o["hx"], non_blocking=True)
+                if o["hres"] is not None:
+                    o["res"].copy_(o["hres"], non_blocking=True)
+                if chain and i + 1 < len(ops) and ops[i + 1]["info"]["prefetch_bytes"] > 0:
+                    side.wait_stream(stream)
+                    ops[i + 1]["plan"].prefetch(ops[i + 1]["W"], side)
+                o["plan"].run(o["x"], o["W"], o["res"], o["y"], stream)
+                if chain and i + 1 < len(ops):
+                    stream.wait_stream(side)
+                o["hy"].copy_(o["y"], non_blocking=True)
+            stream.synchronize()
+        for _ in range(2):
+            e2e_step()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(Ke):
+            e2e_step()
+        te = time.perf_counter() - t0
+        te, eb = aggregate(te, wbytes_step * Ke, world)
+        result["e2e"] = {"value": round(eb / te / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                         "d2h_bytes_per_step": d2h, "steps": Ke,
+                         "ms_per_step": round(te / Ke * 1e3, 4)}
+
+    for o in ops:
+        o["plan"].check()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = OracleSample(hostcopy, args.cpu_seconds)
+        gbs, secs = smp.run()
+        result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": smp.cores, "kind": "oracle",
+                                  "sample": smp.desc, "seconds": round(secs, 2)}
+    for o in ops:
+        o["plan"].close()
+    if world > 1:
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    projs, desc, cfg = workload(args.workload)
+    K = args.steps or 5
+    warm = max(3, args.warmup)
+    smp = OracleSample(host_data(projs), min(20.0, max(0.5, args.ref_seconds / K)))
+    for _ in range(warm):
+        smp.run_rows(16)
+    vals, secs = [], 0.0
+    for _ in range(K):
+        g, dt = smp.run()
+        vals.append(g)
+        secs += dt
+    value = sum(smp.rows * 2 * p.K for p, *_ in smp.data) * K / secs / 1e9 if secs > 0 else statistics.median(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": warm, "ms_per_step": round(secs / K * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, **cfg, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": smp.cores, "kind": "oracle",
+                         "sample": smp.desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (default: about --seconds of work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("sweep", "chain", "wide", "deepk", "pr1"), default="sweep")
+    ap.add_argument("--seconds", type=float, default=3.0, help="target timed-region length")
+    ap.add_argument("--e2e-seconds", type=float, default=1.5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--pdl", type=int, default=1)
+    ap.add_argument("--prefetch", type=float, default=None, help="chain: L2 fraction prefetched")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    args = ap.parse_args(argv)
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        line = json.dumps(res)
+        print(line, flush=True)
+        if args.out:
+            with open(args.out, "a") as f:
+                f.write(line + "\n")
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+/*
+ * skg.h -- C ABI of the skinny decode projection library (libskg.so).
+ *
+ * The library computes the projection of low-batch LLM decode,
+ *
+ *     y[m,n] = sum_k x[m,k] * W[n,k]   (+ residual[m,n])     0 <= m < M <= 64
+ *
+ * with bfloat16 W, x and residual, fp32 accumulation and a bf16 (or fp32)
+ * output, on one NVIDIA GB300 (sm_103a).  Every step runs in the library's
+ * own CUDA kernels; there is no CPU path and no fallback to another kernel.
+ *
+ * Where the operations come from.  The method is described, at paragraph
+ * level and without formulas, by "Hyper Optimizing Kimi K3 in vLLM: Moving
+ * Fast and Responsibly" (vLLM blog, NVIDIA), read here through its deep-notes
+ * page (papercache.org) and its French translation (spke.com, "Hyper
+ * optimisation de Kimi K3 dans vLLM : aller vite et responsablement"):
+ *   [TS] method details 1 / Partie 1 section 1, "Tune shapes for the
+ *        workload": small-matrix kernels at batch 1-2, split-K kernels at
+ *        larger batch, each projection tuned to block sizes that fill the GPU.
+ *   [OC] method details 2 / Partie 1 section 2, "Overlap computation and
+ *        communication": the output projection fused with the attention
+ *        residual add.
+ *   [PF] method details 4 / Partie 1 section 4, "Prefetching upcoming weights
+ *        into cache": small-batch decode is bound by streaming weights from
+ *        HBM; a side-stream kernel preloads the next operation's weights.
+ *   [VC] background 2 "Validate correctness systematically" / Partie 2
+ *        section 3: an activation read was once hoisted above a
+ *        synchronisation wait; early loads were restricted to static weights.
+ *
+ * Conventions shared by every entry point
+ *   - Layouts are dense row-major: W is [N,K] (an nn.Linear weight), x is
+ *     [M,K], residual and y are [M,N].  bf16 tensors are raw 16-bit patterns.
+ *   - Device pointers are CUDA device (or managed) addresses on the current
+ *     device.  x and W must be 16-byte aligned (they are read with TMA and
+ *     16-byte vector loads); residual and y need their element alignment.
+ *   - Streams are cudaStream_t handles passed as void* (NULL = legacy default
+ *     stream).  Launches are asynchronous and stream-ordered.
+ *   - The caller owns every tensor and stream.  The library owns each plan,
+ *     the plan's split-K workspace and counters, and its TMA descriptors.
+ *   - Every call returns a status; none throws across the ABI.  On failure,
+ *     skg_last_error() returns a message for the calling thread.  A rejected
+ *     call launches nothing.
+ */
+#ifndef SKG_H
+#define SKG_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SKG_VERSION 1
+
+/* Symbols of the ABI are exported; everything else in the library is hidden. */
+#if defined(__GNUC__)
+#define SKG_API __attribute__((visibility("default")))
+#else
+#define SKG_API
+#endif
+
+typedef enum skg_status {
+    SKG_OK = 0,
+    SKG_ERR_INVALID_ARG = 1,    /* bad size, NULL where a tensor is needed, bad enum */
+    SKG_ERR_UNSUPPORTED = 2,    /* legal request outside what the library implements */
+    SKG_ERR_ALIGNMENT = 3,      /* a pointer misses its required alignment */
+    SKG_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed (message says which) */
+    SKG_ERR_DEVICE_TIMEOUT = 5  /* a kernel's bounded wait ran out (see skg_plan_check) */
+} skg_status;
+
+typedef enum skg_epilogue {
+    SKG_EPI_BF16 = 0,           /* y = bf16(x.W^T) */
+    SKG_EPI_BF16_RESIDUAL = 1,  /* y = bf16(x.W^T + residual), one rounding [OC] */
+    SKG_EPI_FP32 = 2            /* y = fp32(x.W^T), e.g. router scores */
+} skg_epilogue;
+
+typedef enum skg_kernel_kind {
+    SKG_KERNEL_GEMV = 1,        /* M <= 2: CUDA-core kernel, 16-byte weight loads [TS] */
+    SKG_KERNEL_SPLITK_TC = 2    /* M > 2: TMA + tcgen05 split-K kernel [TS] */
+} skg_kernel_kind;
+
+/* Canonical number of K chunks.  Both kernels cut K into this many chunks
+ * (in 16-byte vectors for GEMV, in 64-wide k-blocks for SPLITK_TC), sum each
+ * chunk from a fresh fp32 accumulator, and combine the chunk sums with one
+ * fixed balanced binary tree.  A split only decides which CTA or warp owns
+ * which subtree, so every allowed split gives bit-identical results. */
+#define SKG_CANONICAL_CHUNKS 16
+
+/* What a plan will launch.  Filled by skg_plan_query and skg_plan_info. */
+typedef struct skg_plan_desc {
+    int kernel_kind;        /* skg_kernel_kind */
+    int M, N, K, epilogue;
+    int split_k;            /* S: CTAs (TC) or warps (GEMV) sharing one output's K range; power of 2 dividing 16 */
+    int tile_n;             /* W rows per output tile: 128 (TC) or rows per CTA group (GEMV) */
+    int m_pad;              /* MMA N (TC: M rounded up to 16) or M (GEMV) */
+    int stages;             /* shared-memory pipeline depth (TC), 0 for GEMV */
+    int grid;               /* CTAs launched */
+    int threads;            /* threads per CTA */
+    int smem_bytes;         /* dynamic shared memory per CTA */
+    int from_table;         /* 1 if (M,N,K,epilogue) hit the measured picker table */
+    size_t workspace_bytes; /* split-K partials + counters owned by the plan */
+    size_t prefetch_bytes;  /* bytes skg_prefetch_l2 touches for this plan's W */
+    int pdl;                /* 1: launched with programmatic dependent launch */
+} skg_plan_desc;
+
+typedef struct skg_plan_s *skg_plan_t;
+
+/*
+ * skg_plan_query -- the kernel choice and launch shape for (M,N,K,epilogue)
+ * on a GPU with num_sms SMs and l2_bytes of L2, without touching any GPU.
+ * [TS]: M <= 2 -> SKG_KERNEL_GEMV, M > 2 -> SKG_KERNEL_SPLITK_TC; inside each
+ * kind the split and pipeline depth come from a table of measured timings
+ * (nearest M for a listed (N,K,epilogue)), else from an occupancy rule.
+ * Constraints: 1 <= M <= 64, N >= 1, K >= 8 and K % 8 == 0, epilogue valid.
+ * Errors: SKG_ERR_INVALID_ARG (sizes, enum, NULL out), SKG_ERR_UNSUPPORTED.
+ */
+SKG_API skg_status skg_plan_query(int M, int N, int K, int epilogue, int num_sms,
+                          size_t l2_bytes, skg_plan_desc *out);
+
+/*
+ * skg_plan -- build a plan for (M,N,K,epilogue) on the current CUDA device.
+ * Picks the kernel as skg_plan_query does, allocates the plan's split-K
+ * workspace (S*M*N fp32 partials plus one counter per 128-row tile, zeroed)
+ * and a mapped host word for device-side error reports.  The plan must be
+ * freed with skg_plan_destroy.  One skg_run of a plan may be in flight at a
+ * time (the workspace is shared); concurrent streams need separate plans.
+ * Errors: as skg_plan_query, plus SKG_ERR_CUDA.  *out is NULL on failure.
+ */
+SKG_API skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out);
+
+/*
+ * skg_plan_force -- debug override of the picker inside the plan's kernel
+ * kind: split_k (power of 2 dividing 16; TC needs 2..16, GEMV 1..8) and, for
+ * TC, stages (2..16, limited by shared memory); 0 keeps the current value.
+ * Reallocates the workspace if it must grow.  Used by tests to run every
+ * allowed split.  Errors: SKG_ERR_INVALID_ARG, SKG_ERR_UNSUPPORTED, SKG_ERR_CUDA.
+ */
+SKG_API skg_status skg_plan_force(skg_plan_t plan, int split_k, int stages);
+
+/*
+ * skg_plan_set_pdl -- 1 (default): launch with programmatic dependent launch,
+ * so a kernel's prologue and its first WEIGHT loads overlap the previous
+ * kernel in the stream; x and residual are read, and y written, only after
+ * griddepcontrol.wait [VC].  0: plain stream-ordered launch.
+ */
+SKG_API skg_status skg_plan_set_pdl(skg_plan_t plan, int enable);
+
+/*
+ * skg_run -- y = x.W^T (+ residual) on `stream`, one kernel launch.
+ *   x        device, bf16 [M,K], 16-byte aligned; read-only
+ *   W        device, bf16 [N,K], 16-byte aligned; read-only (static weight)
+ *   residual device, bf16 [M,N], or NULL; non-NULL iff the plan's epilogue
+ *            is SKG_EPI_BF16_RESIDUAL [OC]
+ *   y        device, [M,N], bf16 (fp32 for SKG_EPI_FP32); must not overlap
+ *            the inputs
+ * Allocates nothing.  Results are bit-identical across runs and across every
+ * allowed split of the plan (see SKG_CANONICAL_CHUNKS).
+ * Errors: SKG_ERR_INVALID_ARG (NULL plan/tensor, residual mismatch),
+ * SKG_ERR_ALIGNMENT, SKG_ERR_DEVICE_TIMEOUT (reported by an earlier launch of
+ * this plan), SKG_ERR_CUDA (descriptor encode or launch failure).
+ */
+SKG_API skg_status skg_run(skg_plan_t plan, const void *x, const void *W,
+                   const void *residual, void *y, void *stream);
+
+/*
+ * skg_prefetch_l2 -- [PF] on `side_stream`, ask the L2 to fetch the first
+ * min(2*N*K, f * L2size) bytes of W_next, the weight of the plan `next`, so
+ * that next's skg_run finds them cached.  f = 0.5 unless changed with
+ * skg_plan_set_prefetch_fraction; the L2 size is queried from the device
+ * when the plan is built.  The kernel only issues bulk L2 prefetches (no
+ * data is written); it may run concurrently with any kernel.
+ * Errors: SKG_ERR_INVALID_ARG, SKG_ERR_ALIGNMENT (W_next), SKG_ERR_CUDA.
+ */
+SKG_API skg_status skg_prefetch_l2(skg_plan_t next, const void *W_next, void *side_stream);
+
+/* Fraction f in [0, 1] of the L2 that skg_prefetch_l2 fills for this plan. */
+SKG_API skg_status skg_plan_set_prefetch_fraction(skg_plan_t plan, double fraction);
+
+/* Copy the plan's launch description into *out. */
+SKG_API skg_status skg_plan_info(skg_plan_t plan, skg_plan_desc *out);
+
+/*
+ * skg_plan_check -- synchronise the plan's last stream and report whether
+ * any of its kernels ran out of a bounded wait since the last check
+ * (SKG_ERR_DEVICE_TIMEOUT; the report is then cleared) or a CUDA error is
+ * pending (SKG_ERR_CUDA).
+ */
+SKG_API skg_status skg_plan_check(skg_plan_t plan);
+
+/* Free the plan, its workspace and descriptors (after its work finished). */
+SKG_API skg_status skg_plan_destroy(skg_plan_t plan);
+
+/*
+ * skg_debug_wait_timeout -- failure-detection self test: launch one CTA that
+ * waits on a shared-memory barrier that nothing ever arrives at, bounded by
+ * timeout_ns of %globaltimer; on expiry the kernel records the timeout in
+ * the plan's error word and returns normally, leaving the context usable.
+ * A following skg_plan_check returns SKG_ERR_DEVICE_TIMEOUT.
+ */
+SKG_API skg_status skg_debug_wait_timeout(skg_plan_t plan, unsigned long long timeout_ns,
+                                  void *stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+SKG_API const char *skg_last_error(void);
+
+/* SKG_VERSION of the loaded library. */
+SKG_API int skg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKG_H */

@@ -1,0 +1,543 @@
+// skg_api.cu -- host side of the C ABI declared in include/skg.h.
+//
+// Plans, the kernel picker, argument checks, the split-K workspace, TMA
+// descriptor encoding and kernel launches.  No computation of the projection
+// happens on the host; a request the kernels cannot serve is rejected with a
+// status, never rerouted.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "skg.h"
+#include "skg_internal.h"
+
+using namespace skg;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+skg_status fail(skg_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+skg_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(SKG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------ picker table
+struct TableRow {
+    int kind, M, N, K, epi, split, stages, grid;
+};
+
+const TableRow kTable[] = {
+#include "skg_plan_table.inc"
+    {0, 0, 0, 0, 0, 0, 0, 0}  // sentinel
+};
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int gemv_rows_per_group(int split) { return (kGemvThreads / 32) / split; }
+
+void fill_gemv(skg_plan_desc *d, int split, int grid, int num_sms)
+{
+    d->kernel_kind = SKG_KERNEL_GEMV;
+    d->split_k = split;
+    d->tile_n = gemv_rows_per_group(split);
+    d->m_pad = d->M;
+    d->stages = 0;
+    d->threads = kGemvThreads;
+    d->smem_bytes = gemv_smem_bytes(d->M, d->K);
+    const int groups = (d->N + d->tile_n - 1) / d->tile_n;
+    if (grid <= 0)
+        grid = std::min(groups, std::max(1, num_sms) * 4);
+    d->grid = std::min(grid, groups);
+    d->workspace_bytes = 0;
+}
+
+void fill_tc(skg_plan_desc *d, int split, int stages)
+{
+    d->kernel_kind = SKG_KERNEL_SPLITK_TC;
+    d->split_k = split;
+    d->tile_n = kTileN;
+    d->m_pad = (d->M + 15) / 16 * 16;
+    const int smax = tc_max_stages(d->m_pad, 232448);
+    d->stages = (stages <= 0 || stages > smax) ? smax : std::max(2, stages);
+    d->threads = kTcThreads;
+    d->smem_bytes = tc_smem_bytes(d->m_pad, d->stages);
+    const int n_tiles = (d->N + kTileN - 1) / kTileN;
+    d->grid = n_tiles * split;
+    d->workspace_bytes = static_cast<size_t>(split) * d->M * d->N * sizeof(float) +
+                         static_cast<size_t>(n_tiles) * sizeof(unsigned int);
+}
+
+const TableRow *table_lookup(int kind, int M, int N, int K, int epi)
+{
+    const TableRow *best = nullptr;
+    double best_d = 1e30;
+    for (const TableRow *r = kTable; r->kind != 0; ++r) {
+        if (r->kind != kind || r->N != N || r->K != K || r->epi != epi)
+            continue;
+        const double dist = std::fabs(std::log2(static_cast<double>(r->M)) - std::log2(static_cast<double>(M)));
+        if (dist < best_d) {
+            best_d = dist;
+            best = r;
+        }
+    }
+    return best;
+}
+
+skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg_plan_desc *d)
+{
+    if (!d)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_query: out is NULL");
+    std::memset(d, 0, sizeof *d);
+    if (M < 1 || M > 64)
+        return fail(SKG_ERR_UNSUPPORTED, "M=%d outside 1..64 (decode batch)", M);
+    if (N < 1)
+        return fail(SKG_ERR_INVALID_ARG, "N=%d must be >= 1", N);
+    if (K < 8 || K % 8 != 0)
+        return fail(SKG_ERR_UNSUPPORTED, "K=%d must be a positive multiple of 8 (16-byte rows)", K);
+    if (epi != SKG_EPI_BF16 && epi != SKG_EPI_BF16_RESIDUAL && epi != SKG_EPI_FP32)
+        return fail(SKG_ERR_INVALID_ARG, "unknown epilogue %d", epi);
+    if (static_cast<long long>(M) * N >= (1ll << 31) || static_cast<long long>(N) * K >= (1ll << 40))
+        return fail(SKG_ERR_UNSUPPORTED, "problem too large");
+    if (num_sms < 1)
+        num_sms = 1;
+    d->M = M;
+    d->N = N;
+    d->K = K;
+    d->epilogue = epi;
+    d->pdl = 1;
+    const size_t wbytes = static_cast<size_t>(N) * K * 2;
+    d->prefetch_bytes = std::min(wbytes, static_cast<size_t>(0.5 * static_cast<double>(l2_bytes))) & ~static_cast<size_t>(15);
+
+    // [TS]: the kernel kind follows the batch size alone.
+    const int kind = (M <= 2) ? SKG_KERNEL_GEMV : SKG_KERNEL_SPLITK_TC;
+    if (kind == SKG_KERNEL_GEMV && gemv_smem_bytes(M, K) > kGemvMaxSmem)
+        return fail(SKG_ERR_UNSUPPORTED, "K=%d too large for the M<=2 kernel (x is staged in shared memory)", K);
+    const TableRow *row = table_lookup(kind, M, N, K, epi);
+    if (kind == SKG_KERNEL_GEMV) {
+        int split, grid = 0;
+        if (row) {
+            split = row->split;
+            grid = row->grid;
+            d->from_table = 1;
+        } else {
+            // enough warps to keep ~32 per SM busy, finer splits for short N
+            split = 1;
+            while (split < 8 && static_cast<long long>(N) * split < 32ll * num_sms * 8 / 2)
+                split *= 2;
+        }
+        fill_gemv(d, split, grid, num_sms);
+    } else {
+        int split, stages = 0;
+        const int n_tiles = (N + kTileN - 1) / kTileN;
+        if (row) {
+            split = row->split;
+            stages = row->stages;
+            d->from_table = 1;
+        } else {
+            // one CTA per SM: the largest split that keeps the grid in one wave
+            split = 2;
+            while (split < kChunks && n_tiles * split * 2 <= num_sms)
+                split *= 2;
+        }
+        fill_tc(d, split, stages);
+    }
+    return SKG_OK;
+}
+
+// --------------------------------------------------------- TMA descriptors
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 row-major [rows, cols] with a box of [box_rows, 64], 128B swizzle,
+// zero fill outside the tensor.
+skg_status encode_2d(CUtensorMap *m, const void *base, int rows, int cols, int box_rows)
+{
+    EncodeTiledFn enc = get_encode();
+    if (!enc)
+        return fail(SKG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(SKG_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for [%d,%d]", (int)r, rows, cols);
+    return SKG_OK;
+}
+
+constexpr int kMapCache = 4;
+
+struct MapCache {
+    const void *ptr[kMapCache] = {};
+    CUtensorMap map[kMapCache];
+    int next = 0;
+
+    skg_status get(const void *base, int rows, int cols, int box_rows, const CUtensorMap **out)
+    {
+        for (int i = 0; i < kMapCache; ++i) {
+            if (ptr[i] == base) {
+                *out = &map[i];
+                return SKG_OK;
+            }
+        }
+        const int slot = next;
+        next = (next + 1) % kMapCache;
+        ptr[slot] = nullptr;
+        skg_status st = encode_2d(&map[slot], base, rows, cols, box_rows);
+        if (st != SKG_OK)
+            return st;
+        ptr[slot] = base;
+        *out = &map[slot];
+        return SKG_OK;
+    }
+    void clear() { std::fill(ptr, ptr + kMapCache, nullptr); }
+};
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+} // namespace
+
+struct skg_plan_s {
+    skg_plan_desc d;
+    int device = 0;
+    int num_sms = 0;
+    size_t l2_bytes = 0;
+    double prefetch_fraction = 0.5;
+    void *ws = nullptr;               // [S*M*N] fp32 partials, then counters
+    size_t ws_cap = 0;
+    unsigned int *err_host = nullptr; // mapped pinned word
+    unsigned int *err_dev = nullptr;
+    cudaStream_t last_stream = nullptr;
+    MapCache wmaps, xmaps;
+};
+
+namespace {
+
+skg_status ensure_workspace(skg_plan_s *p)
+{
+    const size_t need = p->d.workspace_bytes;
+    if (need == 0 || need <= p->ws_cap) {
+        if (need && p->ws) {
+            // counters must start at zero for a new split
+            const size_t n_tiles = (p->d.N + kTileN - 1) / kTileN;
+            const size_t part = need - n_tiles * sizeof(unsigned int);
+            cudaError_t e = cudaMemset(static_cast<char *>(p->ws) + part, 0, n_tiles * sizeof(unsigned int));
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaMemset(counters)");
+        }
+        return SKG_OK;
+    }
+    if (p->ws) {
+        cudaFree(p->ws);
+        p->ws = nullptr;
+        p->ws_cap = 0;
+    }
+    cudaError_t e = cudaMalloc(&p->ws, need);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMalloc(split-K workspace)");
+    e = cudaMemset(p->ws, 0, need);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemset(split-K workspace)");
+    p->ws_cap = need;
+    return SKG_OK;
+}
+
+void refresh_prefetch_bytes(skg_plan_s *p)
+{
+    const size_t wbytes = static_cast<size_t>(p->d.N) * p->d.K * 2;
+    const double want = p->prefetch_fraction * static_cast<double>(p->l2_bytes);
+    p->d.prefetch_bytes = std::min(wbytes, static_cast<size_t>(want)) & ~static_cast<size_t>(15);
+}
+
+} // namespace
+
+extern "C" {
+
+int skg_version(void) { return SKG_VERSION; }
+
+const char *skg_last_error(void) { return g_last_error.c_str(); }
+
+skg_status skg_plan_query(int M, int N, int K, int epilogue, int num_sms, size_t l2_bytes,
+                          skg_plan_desc *out)
+{
+    return query(M, N, K, epilogue, num_sms, l2_bytes, out);
+}
+
+skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out)
+{
+    if (!out)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan: out is NULL");
+    *out = nullptr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    int major = 0, minor = 0, sms = 0, l2 = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+        return fail(SKG_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only",
+                    dev, major, minor);
+    skg_plan_desc d;
+    skg_status st = query(M, N, K, epilogue, sms, static_cast<size_t>(l2), &d);
+    if (st != SKG_OK)
+        return st;
+    skg_plan_s *p = new (std::nothrow) skg_plan_s();
+    if (!p)
+        return fail(SKG_ERR_CUDA, "out of host memory");
+    p->d = d;
+    p->device = dev;
+    p->num_sms = sms;
+    p->l2_bytes = static_cast<size_t>(l2);
+    refresh_prefetch_bytes(p);
+    e = cudaHostAlloc(reinterpret_cast<void **>(&p->err_host), sizeof(unsigned int), cudaHostAllocMapped);
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "cudaHostAlloc(error word)");
+    }
+    *p->err_host = 0;
+    e = cudaHostGetDevicePointer(reinterpret_cast<void **>(&p->err_dev), p->err_host, 0);
+    if (e != cudaSuccess) {
+        cudaFreeHost(p->err_host);
+        delete p;
+        return cuda_fail(e, "cudaHostGetDevicePointer(error word)");
+    }
+    st = ensure_workspace(p);
+    if (st != SKG_OK) {
+        skg_plan_destroy(p);
+        return st;
+    }
+    *out = p;
+    return SKG_OK;
+}
+
+skg_status skg_plan_force(skg_plan_t p, int split_k, int stages)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_force: plan is NULL");
+    skg_plan_desc d = p->d;
+    if (split_k != 0) {
+        if (!is_pow2(split_k) || kChunks % split_k != 0)
+            return fail(SKG_ERR_INVALID_ARG, "split_k=%d must be a power of 2 dividing %d", split_k, kChunks);
+        if (d.kernel_kind == SKG_KERNEL_SPLITK_TC && split_k < 2)
+            return fail(SKG_ERR_UNSUPPORTED, "the tensor-core kernel needs split_k >= 2");
+        if (d.kernel_kind == SKG_KERNEL_GEMV && split_k > 8)
+            return fail(SKG_ERR_UNSUPPORTED, "the GEMV kernel supports split_k <= 8");
+    }
+    if (stages != 0 && (d.kernel_kind != SKG_KERNEL_SPLITK_TC || stages < 2 || stages > 16))
+        return fail(SKG_ERR_INVALID_ARG, "stages=%d invalid for this plan", stages);
+    const int split = split_k ? split_k : d.split_k;
+    if (d.kernel_kind == SKG_KERNEL_GEMV) {
+        fill_gemv(&d, split, 0, p->num_sms);
+    } else {
+        const int st = stages ? stages : d.stages;
+        if (st > tc_max_stages(d.m_pad, 232448))
+            return fail(SKG_ERR_UNSUPPORTED, "stages=%d does not fit in shared memory", st);
+        fill_tc(&d, split, st);
+    }
+    d.from_table = 0;
+    p->d = d;
+    p->wmaps.clear();
+    p->xmaps.clear();
+    return ensure_workspace(p);
+}
+
+skg_status skg_plan_set_pdl(skg_plan_t p, int enable)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_set_pdl: plan is NULL");
+    p->d.pdl = enable ? 1 : 0;
+    return SKG_OK;
+}
+
+skg_status skg_plan_set_prefetch_fraction(skg_plan_t p, double fraction)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_set_prefetch_fraction: plan is NULL");
+    if (!(fraction >= 0.0 && fraction <= 1.0))
+        return fail(SKG_ERR_INVALID_ARG, "prefetch fraction %g outside [0, 1]", fraction);
+    p->prefetch_fraction = fraction;
+    refresh_prefetch_bytes(p);
+    return SKG_OK;
+}
+
+skg_status skg_plan_info(skg_plan_t p, skg_plan_desc *out)
+{
+    if (!p || !out)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_info: NULL argument");
+    *out = p->d;
+    return SKG_OK;
+}
+
+skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *residual, void *y,
+                   void *stream)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_run: plan is NULL");
+    if (!x || !W || !y)
+        return fail(SKG_ERR_INVALID_ARG, "skg_run: x, W and y must be non-NULL");
+    const skg_plan_desc &d = p->d;
+    const bool want_res = d.epilogue == SKG_EPI_BF16_RESIDUAL;
+    if (want_res != (residual != nullptr))
+        return fail(SKG_ERR_INVALID_ARG, want_res ? "skg_run: this plan's epilogue needs a residual"
+                                                  : "skg_run: this plan's epilogue takes no residual");
+    if (!aligned(x, 16) || !aligned(W, 16))
+        return fail(SKG_ERR_ALIGNMENT, "skg_run: x and W must be 16-byte aligned");
+    if (!aligned(y, d.epilogue == SKG_EPI_FP32 ? 4 : 2) || (residual && !aligned(residual, 2)))
+        return fail(SKG_ERR_ALIGNMENT, "skg_run: y / residual miss their element alignment");
+    if (__atomic_load_n(p->err_host, __ATOMIC_ACQUIRE) != 0) {
+        __atomic_store_n(p->err_host, 0u, __ATOMIC_RELEASE);
+        return fail(SKG_ERR_DEVICE_TIMEOUT, "an earlier launch of this plan ran out of a bounded wait");
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (d.kernel_kind == SKG_KERNEL_GEMV) {
+        GemvParams g;
+        g.x = static_cast<const uint4 *>(x);
+        g.W = static_cast<const uint4 *>(W);
+        g.res = static_cast<const uint16_t *>(residual);
+        g.y = y;
+        g.err = p->err_dev;
+        g.M = d.M;
+        g.N = d.N;
+        g.K = d.K;
+        g.nv = d.K / 8;
+        g.split = d.split_k;
+        g.rows_per_group = d.tile_n;
+        g.groups = (d.N + d.tile_n - 1) / d.tile_n;
+        g.epilogue = d.epilogue;
+        e = launch_gemv(g, d.grid, d.pdl != 0, s);
+    } else {
+        const CUtensorMap *mw = nullptr, *mx = nullptr;
+        skg_status st = p->wmaps.get(W, d.N, d.K, kTileN, &mw);
+        if (st != SKG_OK)
+            return st;
+        st = p->xmaps.get(x, d.M, d.K, d.m_pad, &mx);
+        if (st != SKG_OK)
+            return st;
+        const int n_tiles = (d.N + kTileN - 1) / kTileN;
+        TcParams t;
+        t.res = static_cast<const uint16_t *>(residual);
+        t.y = y;
+        t.ws = static_cast<float *>(p->ws);
+        t.counters = reinterpret_cast<unsigned int *>(static_cast<char *>(p->ws) +
+                                                      static_cast<size_t>(d.split_k) * d.M * d.N * sizeof(float));
+        t.err = p->err_dev;
+        t.M = d.M;
+        t.N = d.N;
+        t.K = d.K;
+        t.split = d.split_k;
+        t.nkb = (d.K + kBlockK - 1) / kBlockK;
+        t.n_tiles = n_tiles;
+        t.stages = d.stages;
+        t.epilogue = d.epilogue;
+        t.timeout_ns = kDefaultTimeoutNs;
+        e = launch_splitk_tc(*mw, *mx, t, d.m_pad, d.grid, d.pdl != 0, s);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "skg_run launch");
+    p->last_stream = s;
+    return SKG_OK;
+}
+
+skg_status skg_prefetch_l2(skg_plan_t next, const void *W_next, void *side_stream)
+{
+    if (!next || !W_next)
+        return fail(SKG_ERR_INVALID_ARG, "skg_prefetch_l2: NULL argument");
+    if (!aligned(W_next, 16))
+        return fail(SKG_ERR_ALIGNMENT, "skg_prefetch_l2: W_next must be 16-byte aligned");
+    cudaError_t e = launch_prefetch_l2(W_next, next->d.prefetch_bytes, static_cast<cudaStream_t>(side_stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "skg_prefetch_l2 launch");
+    return SKG_OK;
+}
+
+skg_status skg_plan_check(skg_plan_t p)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_check: plan is NULL");
+    cudaError_t e = p->last_stream ? cudaStreamSynchronize(p->last_stream) : cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "skg_plan_check synchronize");
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "skg_plan_check pending error");
+    const unsigned w = __atomic_exchange_n(p->err_host, 0u, __ATOMIC_ACQ_REL);
+    if (w != 0) {
+        // an aborted split-K run leaves its arrival counters unreset
+        ensure_workspace(p);
+        return fail(SKG_ERR_DEVICE_TIMEOUT, "a kernel of this plan ran out of a bounded wait (bits 0x%x)", w);
+    }
+    return SKG_OK;
+}
+
+skg_status skg_debug_wait_timeout(skg_plan_t p, unsigned long long timeout_ns, void *stream)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_debug_wait_timeout: plan is NULL");
+    if (timeout_ns == 0 || timeout_ns > 10000000000ull)
+        return fail(SKG_ERR_INVALID_ARG, "timeout_ns must be in (0, 10 s]");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_debug_wait(p->err_dev, timeout_ns, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "skg_debug_wait_timeout launch");
+    p->last_stream = s;
+    return SKG_OK;
+}
+
+skg_status skg_plan_destroy(skg_plan_t p)
+{
+    if (!p)
+        return SKG_OK;
+    if (p->ws)
+        cudaFree(p->ws);
+    if (p->err_host)
+        cudaFreeHost(p->err_host);
+    delete p;
+    return SKG_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,88 @@
+// skg_internal.h -- shared between the host ABI (skg_api.cu) and the kernel
+// translation units: launch parameters, the canonical K chunking, and the
+// launcher entry points.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "skg.h"
+
+namespace skg {
+
+constexpr int kChunks = SKG_CANONICAL_CHUNKS;  // leaves of the canonical tree
+constexpr int kTileN = 128;                    // W rows per tcgen05 tile (MMA M)
+constexpr int kBlockK = 64;                    // k per TMA box: 64 bf16 = 128 B
+constexpr int kTcThreads = 320;                // producer, MMA, 8 epilogue warps
+constexpr int kGemvThreads = 256;              // 8 warps
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s bounded waits
+
+// Start of canonical chunk c (0 <= c <= kChunks) when `units` (16-byte
+// vectors for GEMV, 64-wide k-blocks for the tensor-core kernel) are cut into
+// kChunks chunks: the first units % kChunks chunks hold one unit more, so
+// any empty chunks are the last ones.
+__host__ __device__ __forceinline__ int chunk_begin(int c, int units)
+{
+    const int q = units / kChunks, r = units % kChunks;
+    return c * q + (c < r ? c : r);
+}
+
+// Number of non-empty chunks.
+__host__ __device__ __forceinline__ int chunks_present(int units)
+{
+    return units >= kChunks ? kChunks : units;
+}
+
+struct GemvParams {
+    const uint4 *x;         // [M, K/8] 16-byte vectors
+    const uint4 *W;         // [N, K/8]
+    const uint16_t *res;    // [M, N] bf16 bits or null
+    void *y;                // [M, N] bf16 bits or fp32
+    unsigned int *err;      // device-visible error word (mapped host memory)
+    int M, N, K;
+    int nv;                 // K / 8
+    int split;              // warps per output row (1, 2, 4, 8)
+    int rows_per_group;     // 8 / split
+    int groups;             // ceil(N / rows_per_group)
+    int epilogue;           // skg_epilogue
+};
+
+struct TcParams {
+    const uint16_t *res;    // [M, N] bf16 bits or null
+    void *y;                // [M, N]
+    float *ws;              // [S, M, N] fp32 partials (S > 1)
+    unsigned int *counters; // [n_tiles] arrival counters, zero between runs
+    unsigned int *err;      // device-visible error word
+    int M, N, K;
+    int split;              // S: CTAs per output tile (2, 4, 8, 16)
+    int nkb;                // ceil(K / 64)
+    int n_tiles;            // ceil(N / 128)
+    int stages;             // shared-memory pipeline depth
+    int epilogue;
+    unsigned long long timeout_ns;
+};
+
+// Error-word bits written by kernels.
+constexpr unsigned kErrTimeoutProducer = 1u << 0;
+constexpr unsigned kErrTimeoutMma = 1u << 1;
+constexpr unsigned kErrTimeoutEpilogue = 1u << 2;
+constexpr unsigned kErrTimeoutDebug = 1u << 3;
+
+// Shared-memory bytes of the tensor-core kernel for (m_pad, stages).
+int tc_smem_bytes(int m_pad, int stages);
+int gemv_smem_bytes(int M, int K);
+constexpr int kGemvMaxSmem = 200 * 1024;  // x staged in shared memory: M * K * 2 bytes
+int tc_max_stages(int m_pad, int smem_limit);
+
+// Launchers (return the cudaError_t of the launch).
+cudaError_t launch_gemv(const GemvParams &p, int grid, bool pdl, cudaStream_t s);
+cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p,
+                             int m_pad, int grid, bool pdl, cudaStream_t s);
+cudaError_t launch_prefetch_l2(const void *base, size_t bytes, cudaStream_t s);
+cudaError_t launch_debug_wait(unsigned int *err, unsigned long long timeout_ns, cudaStream_t s);
+cudaError_t prepare_kernels();  // one-time attribute setup (max dynamic smem)
+
+} // namespace skg

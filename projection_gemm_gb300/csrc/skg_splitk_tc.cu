@@ -1,0 +1,455 @@
+// skg_splitk_tc.cu -- the split-K tensor-core projection kernel for M > 2.
+//
+// "Hyper Optimizing Kimi K3 in vLLM: Moving Fast and Responsibly", method
+// details 1 "Tune shapes for the workload": at larger batch the projections
+// switch to split-K, spreading the reduction dimension over more workers;
+// method details 2: the output projection is fused with the residual add.
+//
+// Design for sm_103a (swap-AB): the 128 W rows of an output tile are the MMA
+// M dimension, and the M <= 64 decode tokens, padded to m_pad = 16/32/48/64,
+// are the MMA N dimension, so nothing is padded to 128.  Per CTA:
+//   warp 0      TMA producer: W tile [128 x 64] (L2 evict-first) and x tile
+//               [m_pad x 64] (rows >= M zero-filled by TMA) into a ring of
+//               shared-memory stages, 128-byte swizzled;
+//   warp 1      TMEM owner and MMA issuer: one thread issues
+//               tcgen05.mma.kind::f16 (bf16 x bf16 -> fp32) into one of two
+//               TMEM accumulators [128 lanes x m_pad columns];
+//   warps 2..9  epilogue: tcgen05.ld the finished accumulator, combine it in
+//               registers, and finally run the split reduction and output.
+//
+// Reduction order (fixed): K is cut into 16 canonical chunks of 64-wide
+// k-blocks.  Each chunk is summed by the MMA from a fresh accumulator; chunk
+// sums are combined by one balanced binary tree (empty chunks skipped).  The
+// S CTAs of a tile each own an aligned subtree of 16/S chunks and write its
+// value to the plan's fp32 workspace; the last CTA to arrive (an atomic
+// counter picks it; no CTA ever waits for another) combines the S values by
+// the top levels of the same tree, in index order, adds the residual in
+// fp32, rounds once to bf16 and writes y.  Every allowed S gives the same
+// bits, and the arrival order never changes them.
+//
+// Ordering rule of the pages (background 2, the activation read hoisted above
+// a synchronisation wait): under programmatic dependent launch only W tiles
+// are requested before griddepcontrol.wait; x, residual, workspace, counters
+// and y are touched only after it.
+//
+// Every wait is bounded (%globaltimer); on expiry a thread records the
+// timeout in the plan's error word, raises the CTA's abort flag, drains its
+// own asynchronous copies / MMAs, and the CTA frees its TMEM and returns.
+#include <cuda_bf16.h>
+
+#include "skg_internal.h"
+#include "skg_ptx.cuh"
+
+namespace skg {
+namespace {
+
+constexpr uint32_t kWBytes = kTileN * kBlockK * 2;  // 16 KB per stage
+constexpr int kEpiThreads = 256;
+
+template <int MPAD>
+struct TcShape {
+    static constexpr uint32_t kXBytes = MPAD * kBlockK * 2;  // multiple of 1 KB
+    // two accumulators + tree levels 1 and 2, rounded up to a power of two
+    static constexpr uint32_t kTmemCols = (4 * MPAD <= 32) ? 32 : (4 * MPAD <= 64 ? 64 : (4 * MPAD <= 128 ? 128 : 256));
+    static constexpr int kNC = MPAD / 2;                     // columns per epilogue thread
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileN, MPAD);
+};
+
+__device__ __forceinline__ void record_failure(const TcParams &p, volatile int *abort, unsigned bit)
+{
+    *abort = 1;
+    if (p.err)
+        atomicOr(p.err, bit);
+}
+
+__device__ __forceinline__ void epi_bar_sync()
+{
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// Barrier over the 256 epilogue threads that also ANDs a predicate.
+__device__ __forceinline__ bool epi_bar_and(bool v)
+{
+    uint32_t out;
+    asm volatile("{\n\t.reg .pred pi, po;\n\t"
+                 "setp.ne.u32 pi, %1, 0;\n\t"
+                 "bar.red.and.pred po, 1, 256, pi;\n\t"
+                 "selp.u32 %0, 1, 0, po;\n\t}"
+                 : "=r"(out) : "r"(v ? 1u : 0u) : "memory");
+    return out != 0;
+}
+
+__device__ __forceinline__ void store_out(const TcParams &p, int m, int n, float v)
+{
+    const size_t idx = static_cast<size_t>(m) * p.N + n;
+    if (p.epilogue == SKG_EPI_FP32) {
+        static_cast<float *>(p.y)[idx] = v;
+        return;
+    }
+    if (p.epilogue == SKG_EPI_BF16_RESIDUAL)
+        v += __uint_as_float(static_cast<uint32_t>(p.res[idx]) << 16);
+    static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(v);
+}
+
+// Read NC consecutive fp32 columns of this thread's TMEM lane into v.  The
+// empty asm statements after the wait tie every use of the loaded registers
+// to a point after tcgen05.wait::ld.
+template <int NC>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[NC])
+{
+    uint32_t r[NC];
+#pragma unroll
+    for (int j = 0; j < NC / 8; ++j)
+        tmem_ld_x8(taddr + 8 * j, *reinterpret_cast<uint32_t(*)[8]>(&r[8 * j]));
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        asm volatile("" : "+r"(r[c]));
+        v[c] = __uint_as_float(r[c]);
+    }
+}
+
+template <int NC>
+__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)[NC])
+{
+#pragma unroll
+    for (int j = 0; j < NC / 8; ++j) {
+        uint32_t r[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            r[c] = __float_as_uint(v[8 * j + c]);
+        tmem_st_x8(taddr + 8 * j, r);
+    }
+    tmem_wait_st();
+}
+
+template <int MPAD>
+__global__ void __launch_bounds__(kTcThreads, 1)
+splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                 const TcParams p)
+{
+    using Sh = TcShape<MPAD>;
+    constexpr int NC = Sh::kNC;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+
+    const int S = p.stages;
+    uint8_t *sW = smem;
+    uint8_t *sX = smem + S * kWBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sX + S * Sh::kXBytes);
+    uint64_t *empty = full + S;
+    uint64_t *tfull = empty + S;      // [2]
+    uint64_t *tempty = tfull + 2;     // [2]
+    uint64_t *drain = tempty + 2;     // [1]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort, [1] last
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x % p.n_tiles;
+    const int split = blockIdx.x / p.n_tiles;
+    const int L = kChunks / p.split;
+    const int leaf0 = split * L;
+    const int total_present = chunks_present(p.nkb);
+    const int present = max(0, min(L, total_present - leaf0));
+    const int kb_begin = chunk_begin(leaf0, p.nkb);
+    const int nk = chunk_begin(leaf0 + present, p.nkb) - kb_begin;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], kEpiThreads / 32);
+        }
+        mbar_init(drain, 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Sh::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0 && nk > 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            const int pre = nk < S ? nk : S;
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], kWBytes + Sh::kXBytes);
+                tma_load_2d(sW + i * kWBytes, &tmW, &full[i], (kb_begin + i) * kBlockK,
+                            tile * kTileN, pol_w);
+            }
+            pdl_wait();  // activations only from here on
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(sX + i * Sh::kXBytes, &tmX, &full[i], (kb_begin + i) * kBlockK, 0, pol_x);
+            int issued = pre;
+            for (int i = pre; i < nk; ++i) {
+                const int s = i % S;
+                const uint32_t ph = (i / S) & 1;
+                if (!mbar_wait(&empty[s], ph ^ 1, p.timeout_ns, &flags[0])) {
+                    record_failure(p, &flags[0], kErrTimeoutProducer);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], kWBytes + Sh::kXBytes);
+                tma_load_2d(sW + s * kWBytes, &tmW, &full[s], (kb_begin + i) * kBlockK,
+                            tile * kTileN, pol_w);
+                tma_load_2d(sX + s * Sh::kXBytes, &tmX, &full[s], (kb_begin + i) * kBlockK, 0, pol_x);
+                issued = i + 1;
+            }
+            if (flags[0]) {
+                // Abort: let every copy this thread issued land before exit.
+                for (int s = 0; s < S && s < issued; ++s) {
+                    const int last = s + S * ((issued - 1 - s) / S);
+                    volatile int never = 0;
+                    mbar_wait(&full[s], (last / S) & 1, p.timeout_ns, &never);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0 && present > 0) {
+            bool ok = true;
+            int i = 0;
+            for (int pl = 0; pl < present && ok; ++pl) {
+                const int b = pl & 1;
+                const uint32_t u = static_cast<uint32_t>(pl >> 1);
+                if (!mbar_wait(&tempty[b], (u & 1) ^ 1, p.timeout_ns, &flags[0])) {
+                    record_failure(p, &flags[0], kErrTimeoutMma);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(b * MPAD);
+                const int kb0 = chunk_begin(leaf0 + pl, p.nkb);
+                const int kb1 = chunk_begin(leaf0 + pl + 1, p.nkb);
+                for (int kb = kb0; kb < kb1; ++kb, ++i) {
+                    const int s = i % S;
+                    const uint32_t ph = (i / S) & 1;
+                    if (!mbar_wait(&full[s], ph, p.timeout_ns, &flags[0])) {
+                        record_failure(p, &flags[0], kErrTimeoutMma);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_kmajor_sw128(smem_u32(sW + s * kWBytes));
+                    const uint64_t bd = smem_desc_kmajor_sw128(smem_u32(sX + s * Sh::kXBytes));
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 16; ++kk)
+                        tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, Sh::kIdesc,
+                                    (kb > kb0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&empty[s]);
+                }
+                if (ok)
+                    tc_commit(&tfull[b]);
+            }
+            if (!ok) {
+                // Abort: wait for the MMAs already issued before TMEM is freed.
+                tc_commit(drain);
+                volatile int never = 0;
+                mbar_wait(drain, 0, p.timeout_ns, &never);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        pdl_wait();  // residual, workspace, counters and y only from here on
+        const int ew = warp - 2;
+        const int quarter = warp & 3;   // TMEM lanes this warp may access
+        const int half = ew >> 2;       // which half of the m_pad columns
+        const int row = quarter * 32 + lane;
+        const int n = tile * kTileN + row;
+        // this thread's columns: accumulator buffer b, and tree levels 1, 2
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(half * NC);
+        const uint32_t lvl1 = lane_base + 2 * MPAD;
+        const uint32_t lvl2 = lane_base + 3 * MPAD;
+        float st0[NC], cur[NC], tmp[NC];
+        bool ok = true;
+        for (int pl = 0; pl < present; ++pl) {
+            const int b = pl & 1;
+            const uint32_t u = static_cast<uint32_t>(pl >> 1);
+            if (!mbar_wait(&tfull[b], u & 1, p.timeout_ns, &flags[0])) {
+                record_failure(p, &flags[0], kErrTimeoutEpilogue);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_load_cols<NC>(lane_base + static_cast<uint32_t>(b * MPAD), cur);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&tempty[b]);
+            // canonical tree over this CTA's chunks: merge completed pairs.
+            // Level 0 stays in registers, levels 1 and 2 in spare TMEM columns.
+            if (pl & 1) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) cur[c] = st0[c] + cur[c];
+                if (pl & 2) {
+                    tmem_load_cols<NC>(lvl1, tmp);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) cur[c] = tmp[c] + cur[c];
+                    if (pl & 4) {
+                        tmem_load_cols<NC>(lvl2, tmp);
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) cur[c] = tmp[c] + cur[c];
+                    } else {
+                        tmem_store_cols<NC>(lvl2, cur);
+                    }
+                } else {
+                    tmem_store_cols<NC>(lvl1, cur);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) st0[c] = cur[c];
+            }
+        }
+        ok = epi_bar_and(ok && !flags[0]);
+        if (ok) {
+            // value of the subtree: 8 chunks -> cur; else fold the stored
+            // complete blocks from the smallest upwards
+            if (present != 8 && present > 0) {
+                bool have = false;
+                if (present & 1) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) cur[c] = st0[c];
+                    have = true;
+                }
+                if (present & 2) {
+                    tmem_load_cols<NC>(lvl1, tmp);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) cur[c] = have ? tmp[c] + cur[c] : tmp[c];
+                    have = true;
+                }
+                if (present & 4) {
+                    tmem_load_cols<NC>(lvl2, tmp);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) cur[c] = have ? tmp[c] + cur[c] : tmp[c];
+                }
+            }
+            if (present > 0 && n < p.N) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    const int m = half * NC + c;
+                    if (m < p.M)
+                        p.ws[(static_cast<size_t>(split) * p.M + m) * p.N + n] = cur[c];
+                }
+            }
+            __threadfence();
+            epi_bar_sync();
+            if (ew == 0 && lane == 0) {
+                const unsigned old = atomicAdd(&p.counters[tile], 1u);
+                flags[1] = (old == static_cast<unsigned>(p.split - 1)) ? 1 : 0;
+            }
+            epi_bar_sync();
+            if (flags[1]) {
+                __threadfence();
+                const int sp = (total_present + L - 1) / L;  // splits holding a value
+                if (n < p.N) {
+#pragma unroll 1
+                    for (int c = 0; c < NC; ++c) {
+                        const int m = half * NC + c;
+                        if (m >= p.M)
+                            break;
+                        float v[kChunks];
+#pragma unroll
+                        for (int s = 0; s < kChunks; ++s)
+                            v[s] = (s < sp) ? __ldcg(&p.ws[(static_cast<size_t>(s) * p.M + m) * p.N + n])
+                                            : 0.f;
+#pragma unroll
+                        for (int stride = 1; stride < kChunks; stride <<= 1) {
+#pragma unroll
+                            for (int i2 = 0; i2 + stride < kChunks; i2 += 2 * stride) {
+                                if (i2 + stride < sp)
+                                    v[i2] = v[i2] + v[i2 + stride];
+                            }
+                        }
+                        store_out(p, m, n, v[0]);
+                    }
+                }
+                if (ew == 0 && lane == 0)
+                    p.counters[tile] = 0;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Sh::kTmemCols);
+    }
+}
+
+template <int MPAD>
+cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p, int grid,
+                      bool pdl, cudaStream_t s)
+{
+    const int smem = tc_smem_bytes(MPAD, p.stages);
+    static int attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (__atomic_load_n(&attr_set[dev], __ATOMIC_ACQUIRE) < smem) {
+        e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+        if (e != cudaSuccess)
+            return e;
+        __atomic_store_n(&attr_set[dev], 232448, __ATOMIC_RELEASE);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, splitk_tc_kernel<MPAD>, tmW, tmX, p);
+}
+
+} // namespace
+
+int tc_smem_bytes(int m_pad, int stages)
+{
+    // 1 KB alignment slack + stages * (W tile + x tile) + barriers and flags
+    return 1024 + stages * (static_cast<int>(kWBytes) + m_pad * kBlockK * 2) + 8 * (2 * stages + 5) + 16;
+}
+
+int tc_max_stages(int m_pad, int smem_limit)
+{
+    int s = 16;
+    while (s > 2 && tc_smem_bytes(m_pad, s) > smem_limit)
+        --s;
+    return s;
+}
+
+cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p,
+                             int m_pad, int grid, bool pdl, cudaStream_t s)
+{
+    switch (m_pad) {
+    case 16: return launch_tc<16>(tmW, tmX, p, grid, pdl, s);
+    case 32: return launch_tc<32>(tmW, tmX, p, grid, pdl, s);
+    case 48: return launch_tc<48>(tmW, tmX, p, grid, pdl, s);
+    case 64: return launch_tc<64>(tmW, tmX, p, grid, pdl, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+} // namespace skg

@@ -5,14 +5,18 @@ projection's arithmetic.  The test suite hands the same bits to the CUDA
 library and to the CPU oracle, and the benchmark uses the same recipe.
 
 Recipe (stated here once, used everywhere):
-  * a CPU ``torch.Generator`` seeded with ``seed`` draws fp32 ``randn`` in the
-    order x [M,K], W [N,K], residual [M,N], then the outlier-row choice;
+  * ``numpy.random.SeedSequence(seed).spawn(4)`` gives one child sequence
+    each for x [M,K], W [N,K], residual [M,N] and the outlier-row choice;
+    a tensor is cut into 64 row blocks (fewer if it has fewer rows), block i
+    is filled with float32 standard normals by ``Generator(PCG64(child_i))``
+    where child_i is the i-th of ``child.spawn(blocks)``; the blocks are
+    filled by a thread pool, and the result does not depend on its size;
   * x ~ N(0, 1), W ~ N(0, 1/K) (standard deviation 1/sqrt(K)), residual
     ~ N(0, var) with the variance given per workload (1 or 4);
   * each draw is cast to bfloat16 with round-to-nearest-even;
   * outlier channels: floor(N/100) distinct rows of W, picked by
-    ``randperm(N)[:N//100]`` after W is drawn, are multiplied by 16 in bf16,
-    which is exact (a power of two).
+    ``permutation(N)[:N//100]`` after W is drawn, are multiplied by 16 in
+    bf16, which is exact (a power of two).
 
 The pages that describe the method measure a production model
 ("Hyper Optimizing Kimi K3 in vLLM: Moving Fast and Responsibly",
@@ -22,10 +26,13 @@ layer stand in for them.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 from typing import Dict, List, Optional, Tuple
 
+import numpy as np
 import torch
 
 
@@ -71,22 +78,42 @@ class Tensors:
     outlier_rows: Optional[torch.Tensor]
 
 
+_BLOCKS = 64
+
+
+def _fill(job):
+    seq, out = job
+    np.random.Generator(np.random.PCG64(seq)).standard_normal(out.shape, dtype=np.float32, out=out)
+
+
+def _normal_bf16(seq: np.random.SeedSequence, shape, std: float) -> torch.Tensor:
+    rows = shape[0]
+    f = np.empty(shape, dtype=np.float32)
+    nb = max(1, min(_BLOCKS, rows))
+    bounds = [rows * i // nb for i in range(nb + 1)]
+    jobs = [(c, f[bounds[i]:bounds[i + 1]]) for i, c in enumerate(seq.spawn(nb))]
+    if f.size >= (1 << 20):
+        with cf.ThreadPoolExecutor(max_workers=min(nb, os.cpu_count() or 1)) as ex:
+            list(ex.map(_fill, jobs))
+    else:
+        for j in jobs:
+            _fill(j)
+    if std != 1.0:
+        f *= np.float32(std)
+    return torch.from_numpy(f).to(torch.bfloat16)
+
+
 def generate(p: Projection, with_weight: bool = True) -> Tensors:
     """Draw the tensors of ``p`` (CPU, bf16) following the module recipe."""
-    g = torch.Generator().manual_seed(int(p.seed))
-    x = torch.randn(p.M, p.K, generator=g, dtype=torch.float32).to(torch.bfloat16)
-    W = None
-    if with_weight:
-        W = (torch.randn(p.N, p.K, generator=g, dtype=torch.float32)
-             * (1.0 / math.sqrt(p.K))).to(torch.bfloat16)
-    res = None
-    if p.has_residual:
-        res = (torch.randn(p.M, p.N, generator=g, dtype=torch.float32)
-               * math.sqrt(p.residual_var)).to(torch.bfloat16)
+    sx, sw, sr, so = np.random.SeedSequence(int(p.seed)).spawn(4)
+    x = _normal_bf16(sx, (p.M, p.K), 1.0)
+    W = _normal_bf16(sw, (p.N, p.K), 1.0 / math.sqrt(p.K)) if with_weight else None
+    res = _normal_bf16(sr, (p.M, p.N), math.sqrt(p.residual_var)) if p.has_residual else None
     rows = None
     if p.outlier_frac > 0 and W is not None:
         count = int(p.N * p.outlier_frac)
-        rows = torch.randperm(p.N, generator=g)[:count]
+        perm = np.random.Generator(np.random.PCG64(so)).permutation(p.N)
+        rows = torch.from_numpy(perm[:count].astype(np.int64))
         W[rows] = W[rows] * 16
     return Tensors(x=x, W=W, res=res, outlier_rows=rows)
 

@@ -1,0 +1,217 @@
+"""Python binding of libskg.so (see include/skg.h) -- argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does
+nothing but convert arguments: torch tensors become device pointers, streams
+become cudaStream_t handles, statuses become exceptions.  All computation
+happens in the library's CUDA kernels; if the library is missing this module
+raises instead of computing anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libskg.so")
+
+SKG_OK = 0
+SKG_ERR_INVALID_ARG = 1
+SKG_ERR_UNSUPPORTED = 2
+SKG_ERR_ALIGNMENT = 3
+SKG_ERR_CUDA = 4
+SKG_ERR_DEVICE_TIMEOUT = 5
+
+SKG_EPI_BF16 = 0
+SKG_EPI_BF16_RESIDUAL = 1
+SKG_EPI_FP32 = 2
+EPILOGUES = {"bf16": SKG_EPI_BF16, "bf16_residual": SKG_EPI_BF16_RESIDUAL, "fp32": SKG_EPI_FP32}
+
+SKG_KERNEL_GEMV = 1
+SKG_KERNEL_SPLITK_TC = 2
+KERNEL_NAMES = {SKG_KERNEL_GEMV: "gemv", SKG_KERNEL_SPLITK_TC: "splitk_tc"}
+
+# Every symbol include/skg.h declares.
+EXPORTS = (
+    "skg_plan_query", "skg_plan", "skg_plan_force", "skg_plan_set_pdl", "skg_run",
+    "skg_prefetch_l2", "skg_plan_set_prefetch_fraction", "skg_plan_info", "skg_plan_check",
+    "skg_plan_destroy", "skg_debug_wait_timeout", "skg_last_error", "skg_version",
+)
+
+
+class SkgError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"skg status {status}: {message}")
+        self.status = status
+
+
+class skg_plan_desc(ctypes.Structure):
+    _fields_ = [
+        ("kernel_kind", ctypes.c_int), ("M", ctypes.c_int), ("N", ctypes.c_int),
+        ("K", ctypes.c_int), ("epilogue", ctypes.c_int), ("split_k", ctypes.c_int),
+        ("tile_n", ctypes.c_int), ("m_pad", ctypes.c_int), ("stages", ctypes.c_int),
+        ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+        ("from_table", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
+        ("prefetch_bytes", ctypes.c_size_t), ("pdl", ctypes.c_int),
+    ]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["kernel"] = KERNEL_NAMES.get(self.kernel_kind, "?")
+        return d
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libskg.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m projection_gemm_gb300.build` "
+                           "(there is no other implementation of the projection)")
+    lib = ctypes.CDLL(path)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    P = ctypes.POINTER
+    lib.skg_plan_query.argtypes = [i, i, i, i, i, sz, P(skg_plan_desc)]
+    lib.skg_plan.argtypes = [i, i, i, i, P(vp)]
+    lib.skg_plan_force.argtypes = [vp, i, i]
+    lib.skg_plan_set_pdl.argtypes = [vp, i]
+    lib.skg_run.argtypes = [vp, vp, vp, vp, vp, vp]
+    lib.skg_prefetch_l2.argtypes = [vp, vp, vp]
+    lib.skg_plan_set_prefetch_fraction.argtypes = [vp, ctypes.c_double]
+    lib.skg_plan_info.argtypes = [vp, P(skg_plan_desc)]
+    lib.skg_plan_check.argtypes = [vp]
+    lib.skg_plan_destroy.argtypes = [vp]
+    lib.skg_debug_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, vp]
+    for name in EXPORTS:
+        getattr(lib, name).restype = ctypes.c_int
+    lib.skg_last_error.restype = ctypes.c_char_p
+    lib.skg_last_error.argtypes = []
+    lib.skg_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != SKG_OK:
+        raise SkgError(status, load().skg_last_error().decode(errors="replace"))
+
+
+def _epi(epilogue) -> int:
+    return EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def skg_version() -> int:
+    return int(load().skg_version())
+
+
+def skg_last_error() -> str:
+    return load().skg_last_error().decode(errors="replace")
+
+
+def skg_plan_query(M: int, N: int, K: int, epilogue, num_sms: int, l2_bytes: int) -> dict:
+    d = skg_plan_desc()
+    _check(load().skg_plan_query(M, N, K, _epi(epilogue), num_sms, l2_bytes, ctypes.byref(d)))
+    return d.as_dict()
+
+
+def skg_plan(M: int, N: int, K: int, epilogue) -> int:
+    h = ctypes.c_void_p()
+    _check(load().skg_plan(M, N, K, _epi(epilogue), ctypes.byref(h)))
+    return h.value
+
+
+def skg_plan_force(plan: int, split_k: int = 0, stages: int = 0):
+    _check(load().skg_plan_force(plan, split_k, stages))
+
+
+def skg_plan_set_pdl(plan: int, enable: bool):
+    _check(load().skg_plan_set_pdl(plan, 1 if enable else 0))
+
+
+def skg_plan_set_prefetch_fraction(plan: int, fraction: float):
+    _check(load().skg_plan_set_prefetch_fraction(plan, float(fraction)))
+
+
+def skg_plan_info(plan: int) -> dict:
+    d = skg_plan_desc()
+    _check(load().skg_plan_info(plan, ctypes.byref(d)))
+    return d.as_dict()
+
+
+def skg_run(plan: int, x, W, residual, y, stream=None):
+    _check(load().skg_run(plan, _ptr(x), _ptr(W), _ptr(residual), _ptr(y), _stream(stream)))
+
+
+def skg_prefetch_l2(plan_next: int, W_next, side_stream=None):
+    _check(load().skg_prefetch_l2(plan_next, _ptr(W_next), _stream(side_stream)))
+
+
+def skg_plan_check(plan: int):
+    _check(load().skg_plan_check(plan))
+
+
+def skg_plan_destroy(plan: int):
+    _check(load().skg_plan_destroy(plan))
+
+
+def skg_debug_wait_timeout(plan: int, timeout_ns: int, stream=None):
+    _check(load().skg_debug_wait_timeout(plan, int(timeout_ns), _stream(stream)))
+
+
+class Plan:
+    """Owns one skg plan handle; methods forward to the C entry points."""
+
+    def __init__(self, M: int, N: int, K: int, epilogue="bf16"):
+        self.M, self.N, self.K = M, N, K
+        self.epilogue = _epi(epilogue)
+        self.handle = skg_plan(M, N, K, self.epilogue)
+
+    def info(self) -> dict:
+        return skg_plan_info(self.handle)
+
+    def force(self, split_k: int = 0, stages: int = 0):
+        skg_plan_force(self.handle, split_k, stages)
+
+    def set_pdl(self, enable: bool):
+        skg_plan_set_pdl(self.handle, enable)
+
+    def run(self, x, W, residual, y, stream=None):
+        skg_run(self.handle, x, W, residual, y, stream)
+
+    def prefetch(self, W, side_stream=None):
+        skg_prefetch_l2(self.handle, W, side_stream)
+
+    def check(self):
+        skg_plan_check(self.handle)
+
+    def close(self):
+        if self.handle:
+            skg_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

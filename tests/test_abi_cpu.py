@@ -1,0 +1,92 @@
+"""The C ABI on the CPU: it builds, loads, exports what include/skg.h declares,
+and its host-only picker makes the documented choices (no GPU needed)."""
+import os
+import re
+
+import pytest
+
+from projection_gemm_gb300 import build, skg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "skg.h")
+SMS, L2 = 152, 126 * 2 ** 20
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    skg.load()
+
+
+def header_symbols():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"SKG_API\s+[\w\s\*]*?\b(skg_\w+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    hs = header_symbols()
+    assert len(hs) >= 12
+    assert sorted(skg.EXPORTS) == hs
+
+
+def test_library_exports_every_declared_symbol():
+    lib = skg.load()
+    for name in header_symbols():
+        assert hasattr(lib, name), name
+    assert skg.skg_version() == 1
+
+
+def test_library_is_sm103a_only():
+    out = build.ARCH
+    assert out == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+@pytest.mark.parametrize("M", range(1, 65))
+def test_kernel_kind_follows_batch(M):
+    d = skg.skg_plan_query(M, 7168, 7168, "bf16", SMS, L2)
+    assert d["kernel"] == ("gemv" if M <= 2 else "splitk_tc")
+    s = d["split_k"]
+    assert s & (s - 1) == 0 and 16 % s == 0
+    if M > 2:
+        assert s >= 2
+        assert d["m_pad"] == (M + 15) // 16 * 16
+        assert d["grid"] == 56 * s
+        assert d["workspace_bytes"] == s * M * 7168 * 4 + 56 * 4
+        assert d["smem_bytes"] <= 232448
+    else:
+        assert d["workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("N,K,epi", [(384, 7168, "fp32"), (12288, 7168, "bf16"), (7168, 16384, "bf16_residual"),
+                                     (4096, 7168, "bf16"), (1, 8, "bf16"), (129, 72, "bf16_residual")])
+def test_query_shapes(N, K, epi):
+    for M in (1, 2, 3, 16, 64):
+        d = skg.skg_plan_query(M, N, K, epi, SMS, L2)
+        assert d["N"] == N and d["K"] == K and d["epilogue"] == skg.EPILOGUES[epi]
+        assert d["prefetch_bytes"] == min(2 * N * K, L2 // 2) // 16 * 16
+        assert d["grid"] >= 1
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 128, 128, 0), skg.SKG_ERR_UNSUPPORTED),
+    ((65, 128, 128, 0), skg.SKG_ERR_UNSUPPORTED),
+    ((4, 0, 128, 0), skg.SKG_ERR_INVALID_ARG),
+    ((4, 128, 12, 0), skg.SKG_ERR_UNSUPPORTED),
+    ((4, 128, 0, 0), skg.SKG_ERR_UNSUPPORTED),
+    ((4, 128, 128, 3), skg.SKG_ERR_INVALID_ARG),
+    ((1, 128, 200000, 0), skg.SKG_ERR_UNSUPPORTED),
+])
+def test_query_rejections(args, status):
+    with pytest.raises(skg.SkgError) as e:
+        skg.skg_plan_query(*args, SMS, L2)
+    assert e.value.status == status
+    assert skg.skg_last_error()
+
+
+def test_null_arguments_are_rejected():
+    lib = skg.load()
+    assert lib.skg_run(None, None, None, None, None, None) == skg.SKG_ERR_INVALID_ARG
+    assert lib.skg_plan_info(None, None) == skg.SKG_ERR_INVALID_ARG
+    assert lib.skg_plan_destroy(None) == skg.SKG_OK
+    assert lib.skg_plan_query(4, 128, 128, 0, SMS, L2, None) == skg.SKG_ERR_INVALID_ARG
+    assert lib.skg_prefetch_l2(None, None, None) == skg.SKG_ERR_INVALID_ARG

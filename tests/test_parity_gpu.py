@@ -1,0 +1,214 @@
+"""GPU kernels against the CPU oracle, through the C ABI.
+
+Small shapes (the oracle computes every output) span several tiles with
+ragged tails in M, N and K for both kernels and all three epilogues; every
+allowed split must reproduce the default plan's bits exactly.  Full-size
+workloads are checked on sampled outputs the oracle computes one by one.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.oracle as O
+from projection_gemm_gb300 import skg
+from projection_gemm_gb300.inputs import (CHAIN_M, DEEPK_M, SWEEP_M, WIDE_M, Projection, bits,
+                                          chain, deepk, generate, pr1, sweep, wide)
+from tests import tolerance as T
+from tests.gpu_util import DeviceCase, out_bits, out_tensor
+
+pytestmark = pytest.mark.gpu
+
+GEMV_SPLITS = (1, 2, 4, 8)
+TC_SPLITS = (2, 4, 8, 16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from projection_gemm_gb300 import build
+    build.build()
+    skg.load()
+    assert torch.cuda.is_available()
+
+
+def full_check(case: DeviceCase, y_bits, what=""):
+    xb, wb, rb = case.host_bits()
+    y_ref, s1, _ = O.linear(xb, wb, rb)
+    return T.check(y_bits, y_ref, s1, case.p.K, fp32=case.p.epilogue == "fp32", what=what)
+
+
+SMALL = [
+    # GEMV (M <= 2)
+    (1, 1000, 1048, "bf16"), (2, 1000, 1048, "bf16_residual"), (1, 384, 7168, "fp32"),
+    (2, 130, 8, "bf16"), (1, 1, 8, "bf16_residual"), (2, 4096, 520, "fp32"), (1, 3000, 4104, "bf16"),
+    # split-K tensor-core kernel (M > 2)
+    (3, 1000, 1048, "bf16"), (5, 257, 1048, "bf16_residual"), (8, 384, 7168, "fp32"),
+    (16, 1024, 1024, "bf16_residual"), (17, 640, 2056, "bf16"), (33, 300, 200, "bf16"),
+    (48, 1000, 1048, "fp32"), (63, 129, 72, "bf16_residual"), (64, 1000, 1048, "bf16"),
+    (64, 128, 8, "bf16"), (4, 1, 64, "bf16"), (32, 2000, 3080, "bf16_residual"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,epi", SMALL, ids=lambda v: str(v))
+def test_small_shapes_all_splits(M, N, K, epi):
+    p = Projection(M, N, K, epi, seed=1000 + M + N + K, residual_var=1.0)
+    case = DeviceCase(p)
+    try:
+        info = case.plan.info()
+        assert info["kernel"] == ("gemv" if M <= 2 else "splitk_tc")
+        base = case.run_bits()
+        full_check(case, base, what=f"{p} default split {info['split_k']}")
+        for s in (GEMV_SPLITS if M <= 2 else TC_SPLITS):
+            case.plan.force(split_k=s)
+            got = case.run_bits()
+            assert np.array_equal(got, base), f"split {s} changed the bits of {p}"
+    finally:
+        case.close()
+
+
+def test_pr1_config():
+    p = pr1()
+    case = DeviceCase(p)
+    try:
+        assert case.plan.info()["kernel"] == "gemv"
+        y = case.run_bits()
+        r = full_check(case, y, what="PR1")
+        assert r <= 1.0
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("M", (1, 2, 8, 64))
+def test_determinism_20_runs(M):
+    case = DeviceCase(Projection(M, 7168, 7168, "bf16", seed=77))
+    try:
+        first = case.run_bits()
+        for _ in range(19):
+            assert np.array_equal(case.run_bits(), first)
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("M", (1, 8, 64))
+@pytest.mark.parametrize("kind", ("identity", "permutation"))
+def test_closed_forms_bit_exact(M, kind):
+    K = 1024
+    g = torch.Generator().manual_seed(5 + M)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    if kind == "identity":
+        W = torch.eye(K, dtype=torch.bfloat16)
+        want = bits(x)
+    else:
+        perm = torch.randperm(K, generator=g)
+        W = torch.zeros(K, K, dtype=torch.bfloat16)
+        W[torch.arange(K), perm] = 1
+        want = bits(x[:, perm])
+    from projection_gemm_gb300.inputs import Tensors
+    case = DeviceCase(Projection(M, K, K, "bf16"), Tensors(x=x, W=W, res=None, outlier_rows=None))
+    try:
+        assert np.array_equal(case.run_bits(), want)
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("M", (1, 2, 16, 64))
+def test_zero_weight_gives_residual_exactly(M):
+    from projection_gemm_gb300.inputs import Tensors
+    N, K = 700, 520
+    g = torch.Generator().manual_seed(M)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    res = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    W = torch.zeros(N, K, dtype=torch.bfloat16)
+    case = DeviceCase(Projection(M, N, K, "bf16_residual"), Tensors(x=x, W=W, res=res, outlier_rows=None))
+    try:
+        assert np.array_equal(case.run_bits(), bits(res))
+    finally:
+        case.close()
+
+
+def _sampled_check(p: Projection, npts=3000, extra_rows=()):
+    t = generate(p)
+    case = DeviceCase(p, t)
+    try:
+        y = case.run_bits()
+        rng = np.random.default_rng(p.seed)
+        ns = np.concatenate([rng.integers(0, p.N, npts), [0, p.N - 1], np.asarray(extra_rows, dtype=np.int64)])
+        ms = np.concatenate([rng.integers(0, p.M, npts), [p.M - 1, 0], rng.integers(0, p.M, len(extra_rows))])
+        xb, wb, rb = case.host_bits()
+        y_ref, s1 = O.linear_points(xb, wb, ms, ns, rb)
+        return T.check(y[ms, ns], y_ref, s1, p.K, fp32=p.epilogue == "fp32", what=p.name), case.plan.info()
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("M", SWEEP_M)
+def test_sweep_full_size_sampled(M):
+    ratio, info = _sampled_check(sweep(M))
+    assert info["kernel"] == ("gemv" if M <= 2 else "splitk_tc")
+
+
+@pytest.mark.parametrize("M", WIDE_M)
+def test_wide_full_size_sampled(M):
+    p = wide(M)
+    t = generate(p)
+    _sampled_check(p, extra_rows=t.outlier_rows[:50].numpy())
+
+
+@pytest.mark.parametrize("M", DEEPK_M)
+def test_deepk_residual_full_size_sampled(M):
+    _sampled_check(deepk(M))
+
+
+@pytest.mark.parametrize("M", CHAIN_M)
+def test_chain_stages_full_size_sampled(M):
+    for p in chain(M):
+        _sampled_check(p, npts=1500)
+
+
+@pytest.mark.parametrize("M", (8, 64))
+def test_full_size_splits_bit_identical(M):
+    case = DeviceCase(sweep(M))
+    try:
+        base = case.run_bits()
+        for s in TC_SPLITS:
+            case.plan.force(split_k=s)
+            assert np.array_equal(case.run_bits(), base), f"split {s}"
+    finally:
+        case.close()
+
+
+def test_full_oracle_sweep_m16():
+    """One full-size launch checked on every output."""
+    case = DeviceCase(sweep(16))
+    try:
+        full_check(case, case.run_bits(), what="sweep M=16 all outputs")
+    finally:
+        case.close()
+
+
+# ---------------------------------------------------------------- errors
+def test_rejections_launch_nothing():
+    p = skg.Plan(4, 256, 256, "bf16")
+    try:
+        x = torch.zeros(4 * 256 + 8, dtype=torch.bfloat16, device="cuda")
+        W = torch.zeros(256, 256, dtype=torch.bfloat16, device="cuda")
+        y = torch.zeros(4, 256, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(skg.SkgError) as e:
+            p.run(x.data_ptr() + 2, W, None, y)
+        assert e.value.status == skg.SKG_ERR_ALIGNMENT
+        with pytest.raises(skg.SkgError) as e:
+            p.run(x, W, y, y)
+        assert e.value.status == skg.SKG_ERR_INVALID_ARG
+        with pytest.raises(skg.SkgError) as e:
+            p.run(x, 0, None, y)
+        assert e.value.status == skg.SKG_ERR_INVALID_ARG
+    finally:
+        p.close()
+    for bad in ((0, 128, 128), (65, 128, 128), (4, 0, 128), (4, 128, 12), (4, 128, 0)):
+        with pytest.raises(skg.SkgError):
+            skg.Plan(*bad, "bf16")
+    with pytest.raises(skg.SkgError):
+        skg.Plan(4, 128, 128, 7)
