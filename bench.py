@@ -242,12 +242,14 @@ def run_ours(args):
                         hx=t.x.pin_memory(), hres=None if t.res is None else t.res.pin_memory(),
                         hy=torch.empty(p.M, p.N, dtype=dt).pin_memory()))
         del t
-    chain = args.workload == "chain"
+    # [PF] the next projection's weight is prefetched into L2 on a side stream
+    # while the current one runs (default: the chain; any workload with --prefetch)
+    chain = args.workload == "chain" if args.prefetch is None else args.prefetch > 0
     side = torch.cuda.Stream(device=dev)
     stream = torch.cuda.current_stream(dev)
-    if chain and args.prefetch is not None:
+    if args.prefetch is not None:
         for o in ops:
-            skg.skg_plan_set_prefetch_fraction(o["plan"].handle, args.prefetch)
+            skg.skg_plan_set_prefetch_fraction(o["plan"].handle, max(0.0, args.prefetch))
 
     def step(events=None):
         for i, o in enumerate(ops):
@@ -343,7 +345,9 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": desc, **cfg, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": ("inputs larger than L2: every step streams %.1f MB of distinct weights" % (wbytes_step / 1e6)),
-                   "pdl": bool(args.pdl)},
+                   "pdl": bool(args.pdl),
+                   "prefetch_fraction": (ops[0]["plan"].info()["prefetch_bytes"] and
+                                         (args.prefetch if args.prefetch is not None else 0.5)) if chain else 0.0},
         "per_projection": per_m, "roofline": roofline,
         "gpu_launches": launches_per_step * K,
     }
@@ -436,7 +440,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--pdl", type=int, default=1)
-    ap.add_argument("--prefetch", type=float, default=None, help="chain: L2 fraction prefetched")
+    ap.add_argument("--prefetch", type=float, default=None,
+                    help="fraction of L2 filled with the next weight on a side stream (default: 0.5 for the chain, off otherwise)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -93,7 +93,8 @@ typedef struct skg_plan_desc {
     int split_k;            /* S: CTAs (TC) or warps (GEMV) sharing one output's K range; power of 2 dividing 16 */
     int tile_n;             /* W rows per output tile: 128 (TC) or rows per CTA group (GEMV) */
     int m_pad;              /* MMA N (TC: M rounded up to 16) or M (GEMV) */
-    int stages;             /* shared-memory pipeline depth (TC), 0 for GEMV */
+    int stages;             /* TC: shared-memory ring stages; GEMV: weight-ring slots per warp */
+    int tma_burst;          /* TC: k-blocks the TMA producer requests back to back */
     int grid;               /* CTAs launched */
     int threads;            /* threads per CTA */
     int smem_bytes;         /* dynamic shared memory per CTA */
@@ -129,13 +130,18 @@ SKG_API skg_status skg_plan_query(int M, int N, int K, int epilogue, int num_sms
 SKG_API skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out);
 
 /*
- * skg_plan_force -- debug override of the picker inside the plan's kernel
- * kind: split_k (power of 2 dividing 16; TC needs 2..16, GEMV 1..8) and, for
- * TC, stages (2..16, limited by shared memory); 0 keeps the current value.
- * Reallocates the workspace if it must grow.  Used by tests to run every
- * allowed split.  Errors: SKG_ERR_INVALID_ARG, SKG_ERR_UNSUPPORTED, SKG_ERR_CUDA.
+ * skg_plan_force -- override of the picker inside the plan's kernel kind
+ * (used by tests and by the tuning sweep): split_k (power of 2 dividing 16;
+ * TC needs 2..16, GEMV 1..8); for TC, stages (2..16, limited by shared
+ * memory) and tma_burst (1..stages); for GEMV, grid (CTAs, >= 1).  A 0 keeps
+ * the current value; a field that does not apply to the kind must be 0.
+ * If the workspace must grow, a new one is allocated and the old one is kept
+ * until skg_plan_destroy, because a CUDA graph that captured skg_run of this
+ * plan earlier still launches with the captured split, descriptors and
+ * workspace.  Used by tests to run every allowed split.  Errors: SKG_ERR_INVALID_ARG, SKG_ERR_UNSUPPORTED, SKG_ERR_CUDA.
  */
-SKG_API skg_status skg_plan_force(skg_plan_t plan, int split_k, int stages);
+SKG_API skg_status skg_plan_force(skg_plan_t plan, int split_k, int stages, int grid,
+                                  int tma_burst);
 
 /*
  * skg_plan_set_pdl -- 1 (default): launch with programmatic dependent launch,

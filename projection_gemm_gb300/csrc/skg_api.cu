@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,44 +44,81 @@ skg_status cuda_fail(cudaError_t e, const char *what)
 
 // ------------------------------------------------------------ picker table
 struct TableRow {
-    int kind, M, N, K, epi, split, stages, grid;
+    int kind, M, N, K, epi, split, stages, grid, burst;
 };
 
 const TableRow kTable[] = {
 #include "skg_plan_table.inc"
-    {0, 0, 0, 0, 0, 0, 0, 0}  // sentinel
+    {0, 0, 0, 0, 0, 0, 0, 0, 0}  // sentinel
 };
 
 bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
 int gemv_rows_per_group(int split) { return (kGemvThreads / 32) / split; }
 
-void fill_gemv(skg_plan_desc *d, int split, int grid, int num_sms)
+// Ring depth for the M <= 2 kernel: the deepest ring (<= 9 slots) with which
+// two CTAs share an SM, else one CTA; 0 if even a 2-slot ring does not fit.
+int gemv_default_ring(int M, int K, int split, int *ctas)
+{
+    for (int c = 2; c >= 1; --c) {
+        const int budget = 233472 / c - 1024;   // 228 KB per SM, 1 KB reserved per CTA
+        int r = 9;
+        while (r >= 3 && gemv_smem_bytes(M, K, split, r) > std::min(budget, kGemvMaxSmem))
+            --r;
+        if (r >= 3) {
+            *ctas = c;
+            return r;
+        }
+    }
+    *ctas = 1;
+    return gemv_smem_bytes(M, K, split, 2) <= kGemvMaxSmem ? 2 : 0;
+}
+
+void fill_gemv(skg_plan_desc *d, int split, int ring, int grid, int num_sms)
 {
     d->kernel_kind = SKG_KERNEL_GEMV;
     d->split_k = split;
-    d->tile_n = gemv_rows_per_group(split);
     d->m_pad = d->M;
-    d->stages = 0;
+    d->workspace_bytes = 0;
+    d->tma_burst = 0;
     d->threads = kGemvThreads;
-    d->smem_bytes = gemv_smem_bytes(d->M, d->K);
+    if (split == 1) {
+        // whole rows per warp: tile_n = rows per CTA = 8 warps x rows per warp
+        const int warps = kGemvThreads / 32;
+        int rpw = 1;
+        if (grid > 0)
+            rpw = std::max(1, (d->N + warps * grid - 1) / (warps * grid));
+        d->tile_n = warps * rpw;
+        d->stages = 0;
+        d->smem_bytes = gemv_smem_bytes(d->M, d->K, 1, 0);
+        d->grid = (d->N + d->tile_n - 1) / d->tile_n;
+        return;
+    }
+    d->tile_n = gemv_rows_per_group(split);
+    int ctas = 1;
+    const int r0 = gemv_default_ring(d->M, d->K, split, &ctas);
+    d->stages = ring > 0 ? ring : r0;
+    d->tma_burst = 0;
+    d->threads = kGemvThreads;
+    d->smem_bytes = gemv_smem_bytes(d->M, d->K, split, d->stages);
     const int groups = (d->N + d->tile_n - 1) / d->tile_n;
     if (grid <= 0)
-        grid = std::min(groups, std::max(1, num_sms) * 4);
+        grid = std::max(1, num_sms) * ctas;
     d->grid = std::min(grid, groups);
     d->workspace_bytes = 0;
 }
 
-void fill_tc(skg_plan_desc *d, int split, int stages)
+void fill_tc(skg_plan_desc *d, int split, int stages, int burst)
 {
     d->kernel_kind = SKG_KERNEL_SPLITK_TC;
     d->split_k = split;
     d->tile_n = kTileN;
     d->m_pad = (d->M + 15) / 16 * 16;
     const int smax = tc_max_stages(d->m_pad, 232448);
-    d->stages = (stages <= 0 || stages > smax) ? smax : std::max(2, stages);
+    d->stages = stages <= 0 ? std::min(kTcDefaultStages, smax) : std::max(2, std::min(stages, smax));
     d->threads = kTcThreads;
     d->smem_bytes = tc_smem_bytes(d->m_pad, d->stages);
+    d->tma_burst = std::max(1, std::min(burst, d->stages));
     const int n_tiles = (d->N + kTileN - 1) / kTileN;
     d->grid = n_tiles * split;
     d->workspace_bytes = static_cast<size_t>(split) * d->M * d->N * sizeof(float) +
@@ -130,36 +168,49 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
 
     // [TS]: the kernel kind follows the batch size alone.
     const int kind = (M <= 2) ? SKG_KERNEL_GEMV : SKG_KERNEL_SPLITK_TC;
-    if (kind == SKG_KERNEL_GEMV && gemv_smem_bytes(M, K) > kGemvMaxSmem)
+    if (kind == SKG_KERNEL_GEMV && gemv_smem_bytes(M, K, 1, 0) > kGemvMaxSmem)
         return fail(SKG_ERR_UNSUPPORTED, "K=%d too large for the M<=2 kernel (x is staged in shared memory)", K);
     const TableRow *row = table_lookup(kind, M, N, K, epi);
     if (kind == SKG_KERNEL_GEMV) {
-        int split, grid = 0;
+        int split, grid = 0, ring = 0;
         if (row) {
             split = row->split;
             grid = row->grid;
+            ring = row->stages;
             d->from_table = 1;
+        } else if (N >= 4096) {
+            split = 1;   // enough rows for one warp per row
         } else {
-            // enough warps to keep ~32 per SM busy, finer splits for short N
-            split = 1;
-            while (split < 8 && static_cast<long long>(N) * split < 32ll * num_sms * 8 / 2)
+            // short N: warps share rows; the smallest split whose per-warp K
+            // slice fits 4-strip ring slots, then finer while N is short
+            split = 2;
+            while (split < 8 && gemv_strips_per_warp(K, split) > 4)
+                split *= 2;
+            while (split < 8 && static_cast<long long>(N) * split < 48ll * num_sms)
                 split *= 2;
         }
-        fill_gemv(d, split, grid, num_sms);
+        if (split > 1 && (gemv_strips_per_warp(K, split) > 16 || gemv_smem_bytes(M, K, split, 2) > kGemvMaxSmem))
+            split = 1;   // K too long for the shared rows' ring
+        fill_gemv(d, split, ring, grid, num_sms);
+        if (split > 1 && d->stages < 2)
+            return fail(SKG_ERR_UNSUPPORTED, "M=%d K=%d does not fit the M<=2 kernel's shared memory", M, K);
     } else {
-        int split, stages = 0;
+        int split, stages = 0, burst = 1;
         const int n_tiles = (N + kTileN - 1) / kTileN;
         if (row) {
             split = row->split;
             stages = row->stages;
+            burst = row->burst;
             d->from_table = 1;
         } else {
-            // one CTA per SM: the largest split that keeps the grid in one wave
+            // the largest split that keeps every CTA resident in one wave
+            const int mp = (M + 15) / 16 * 16;
+            const int slots = num_sms * tc_ctas_per_sm(mp, std::min(kTcDefaultStages, tc_max_stages(mp, 232448)));
             split = 2;
-            while (split < kChunks && n_tiles * split * 2 <= num_sms)
+            while (split < kChunks && n_tiles * split * 2 <= slots)
                 split *= 2;
         }
-        fill_tc(d, split, stages);
+        fill_tc(d, split, stages, burst);
     }
     return SKG_OK;
 }
@@ -244,6 +295,8 @@ struct skg_plan_s {
     double prefetch_fraction = 0.5;
     void *ws = nullptr;               // [S*M*N] fp32 partials, then counters
     size_t ws_cap = 0;
+    std::vector<void *> retired;      // outgrown workspaces: a captured graph may still use them
+    int gemv_ctas_per_sm = 0;         // measured occupancy of the GEMV kernel
     unsigned int *err_host = nullptr; // mapped pinned word
     unsigned int *err_dev = nullptr;
     cudaStream_t last_stream = nullptr;
@@ -267,7 +320,9 @@ skg_status ensure_workspace(skg_plan_s *p)
         return SKG_OK;
     }
     if (p->ws) {
-        cudaFree(p->ws);
+        // Not freed here: a CUDA graph captured earlier may still launch with
+        // this pointer.  Released by skg_plan_destroy.
+        p->retired.push_back(p->ws);
         p->ws = nullptr;
         p->ws_cap = 0;
     }
@@ -333,6 +388,19 @@ skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out)
     p->num_sms = sms;
     p->l2_bytes = static_cast<size_t>(l2);
     refresh_prefetch_bytes(p);
+    if (p->d.kernel_kind == SKG_KERNEL_GEMV) {
+        e = gemv_occupancy(M, K, p->d.split_k, p->d.stages, &p->gemv_ctas_per_sm);
+        if (e != cudaSuccess) {
+            delete p;
+            return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        }
+        if (p->gemv_ctas_per_sm < 1) {
+            delete p;
+            return fail(SKG_ERR_UNSUPPORTED, "the M<=2 kernel cannot be resident with this shape");
+        }
+        if (p->d.split_k > 1 && (!p->d.from_table || p->d.grid <= 0))
+            fill_gemv(&p->d, p->d.split_k, p->d.stages, sms * p->gemv_ctas_per_sm, sms);
+    }
     e = cudaHostAlloc(reinterpret_cast<void **>(&p->err_host), sizeof(unsigned int), cudaHostAllocMapped);
     if (e != cudaSuccess) {
         delete p;
@@ -354,7 +422,7 @@ skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out)
     return SKG_OK;
 }
 
-skg_status skg_plan_force(skg_plan_t p, int split_k, int stages)
+skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int tma_burst)
 {
     if (!p)
         return fail(SKG_ERR_INVALID_ARG, "skg_plan_force: plan is NULL");
@@ -362,21 +430,49 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages)
     if (split_k != 0) {
         if (!is_pow2(split_k) || kChunks % split_k != 0)
             return fail(SKG_ERR_INVALID_ARG, "split_k=%d must be a power of 2 dividing %d", split_k, kChunks);
+        if (d.kernel_kind == SKG_KERNEL_GEMV && split_k > 1 && gemv_strips_per_warp(d.K, split_k) > 16)
+            return fail(SKG_ERR_UNSUPPORTED, "split_k=%d leaves more than 16 strips per warp at K=%d", split_k, d.K);
         if (d.kernel_kind == SKG_KERNEL_SPLITK_TC && split_k < 2)
             return fail(SKG_ERR_UNSUPPORTED, "the tensor-core kernel needs split_k >= 2");
         if (d.kernel_kind == SKG_KERNEL_GEMV && split_k > 8)
             return fail(SKG_ERR_UNSUPPORTED, "the GEMV kernel supports split_k <= 8");
     }
-    if (stages != 0 && (d.kernel_kind != SKG_KERNEL_SPLITK_TC || stages < 2 || stages > 16))
+    if (stages != 0 && (stages < 2 || stages > (d.kernel_kind == SKG_KERNEL_GEMV ? 9 : 16)))
         return fail(SKG_ERR_INVALID_ARG, "stages=%d invalid for this plan", stages);
+    if (tma_burst != 0 && (d.kernel_kind != SKG_KERNEL_SPLITK_TC || tma_burst < 1))
+        return fail(SKG_ERR_INVALID_ARG, "tma_burst=%d invalid for this plan", tma_burst);
+    if (grid != 0 && (d.kernel_kind != SKG_KERNEL_GEMV || grid < 1))
+        return fail(SKG_ERR_INVALID_ARG, "grid=%d invalid for this plan", grid);
     const int split = split_k ? split_k : d.split_k;
-    if (d.kernel_kind == SKG_KERNEL_GEMV) {
-        fill_gemv(&d, split, 0, p->num_sms);
+    if (d.kernel_kind == SKG_KERNEL_GEMV && split == 1) {
+        if (stages)
+            return fail(SKG_ERR_INVALID_ARG, "split_k=1 (whole rows per warp) has no weight ring");
+        fill_gemv(&d, 1, 0, grid, p->num_sms);
+    } else if (d.kernel_kind == SKG_KERNEL_GEMV) {
+        int ctas = 1;
+        int ring = stages ? stages : ((split_k || d.stages < 2) ? gemv_default_ring(d.M, d.K, split, &ctas) : d.stages);
+        if (ring < 2 || gemv_smem_bytes(d.M, d.K, split, ring) > kGemvMaxSmem)
+            return fail(SKG_ERR_UNSUPPORTED, "a %d-slot ring does not fit shared memory at split %d", ring, split);
+        int g = grid ? grid : d.grid;
+        if ((split_k || stages || d.split_k == 1) && !grid) {
+            int occ = 1;
+            cudaError_t e = gemv_occupancy(d.M, d.K, split, ring, &occ);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+            if (occ < 1)
+                return fail(SKG_ERR_UNSUPPORTED, "this GEMV configuration cannot be resident");
+            p->gemv_ctas_per_sm = occ;
+            g = p->num_sms * occ;
+        }
+        fill_gemv(&d, split, ring, g, p->num_sms);
     } else {
         const int st = stages ? stages : d.stages;
         if (st > tc_max_stages(d.m_pad, 232448))
             return fail(SKG_ERR_UNSUPPORTED, "stages=%d does not fit in shared memory", st);
-        fill_tc(&d, split, st);
+        const int b = tma_burst ? tma_burst : d.tma_burst;
+        if (b > st)
+            return fail(SKG_ERR_INVALID_ARG, "tma_burst=%d exceeds stages=%d", b, st);
+        fill_tc(&d, split, st, b);
     }
     d.from_table = 0;
     p->d = d;
@@ -448,6 +544,8 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         g.split = d.split_k;
         g.rows_per_group = d.tile_n;
         g.groups = (d.N + d.tile_n - 1) / d.tile_n;
+        g.ring = d.stages;
+        g.rows_per_warp = d.split_k == 1 ? d.tile_n / (kGemvThreads / 32) : 0;
         g.epilogue = d.epilogue;
         e = launch_gemv(g, d.grid, d.pdl != 0, s);
     } else {
@@ -473,6 +571,7 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         t.nkb = (d.K + kBlockK - 1) / kBlockK;
         t.n_tiles = n_tiles;
         t.stages = d.stages;
+        t.burst = d.tma_burst;
         t.epilogue = d.epilogue;
         t.timeout_ns = kDefaultTimeoutNs;
         e = launch_splitk_tc(*mw, *mx, t, d.m_pad, d.grid, d.pdl != 0, s);
@@ -534,6 +633,8 @@ skg_status skg_plan_destroy(skg_plan_t p)
         return SKG_OK;
     if (p->ws)
         cudaFree(p->ws);
+    for (void *w : p->retired)
+        cudaFree(w);
     if (p->err_host)
         cudaFreeHost(p->err_host);
     delete p;

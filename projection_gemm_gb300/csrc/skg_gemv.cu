@@ -9,12 +9,14 @@
 // lane are in flight before any is used, and accumulation is fp32 on CUDA
 // cores -- tensor cores would idle at this arithmetic intensity.
 //
-// Reduction order (fixed, independent of the launch shape): row n's K range
-// is cut into 16 canonical chunks of 16-byte vectors; inside chunk c, lane l
-// accumulates vectors begin(c) + l + 32 j for j = 0, 1, ... in order, each
-// vector's 8 products in element order with fp32 FMA; the 32 lane sums are
-// combined by the xor butterfly 16, 8, 4, 2, 1; the 16 chunk sums are
-// combined by one balanced binary tree (empty chunks skipped).  A split of
+// Reduction order (fixed, independent of the launch shape): row n is read in
+// strips of 32 16-byte vectors (one coalesced 512-byte warp load; lane l
+// takes vector 32 t + l of strip t).  The strips are cut into 16 canonical
+// chunks of J = ceil(strips / 16) consecutive strips (the last chunks may be
+// short or empty).  Inside a chunk each lane accumulates its vectors in strip
+// order, each vector's 8 products in element order with fp32 FMA; the 32 lane
+// sums are combined by the xor butterfly 16, 8, 4, 2, 1; the 16 chunk sums
+// are combined by one balanced binary tree (empty chunks skipped).  A split of
 // `split` warps per row hands each warp an aligned subtree of 16/split
 // chunks, so every split gives the same bits.
 #include <cuda_bf16.h>
@@ -89,6 +91,17 @@ __device__ __forceinline__ void fma8(float &acc, uint4 xv, uint4 wv)
     acc = fmaf(bf16hi(xv.w), bf16hi(wv.w), acc);
 }
 
+// 16-byte shared-memory load of an x vector; volatile so the compiler does
+// not hoist the (loop-invariant) x slice into registers for the whole kernel.
+__device__ __forceinline__ uint4 lds_v4(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+    return v;
+}
+
 __device__ __forceinline__ void store_out(const GemvParams &p, int m, int n, float v)
 {
     const size_t idx = static_cast<size_t>(m) * p.N + n;
@@ -101,12 +114,18 @@ __device__ __forceinline__ void store_out(const GemvParams &p, int m, int n, flo
     static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(v);
 }
 
-// U = 16-byte weight vectors each lane keeps in flight per batch.  x is
-// staged once per CTA in shared memory (dynamic, M * K * 2 bytes).
-template <int MM, int U>
+// T = the most strips one warp reads per row.  Weights land in shared
+// memory: every warp owns a ring of p.ring slots of T strips (T * 512 bytes)
+// and keeps p.ring - 1 rows of its K slice in flight with per-lane 16-byte
+// cp.async copies (L2 evict-first).  Each lane later reads back exactly the
+// vectors it copied itself, so per-thread wait_group is the only
+// synchronisation the ring needs.  x is staged once per CTA in shared memory;
+// the grid is persistent.
+template <int MM, int T>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p)
 {
-    extern __shared__ uint4 xs[];                 // [MM][nv]
+    extern __shared__ uint4 dsm[];
+    uint4 *xs = dsm;                              // [MM][nv]
     __shared__ float part[2][kWarps][MM];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -114,107 +133,84 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p)
     const int row_in_group = warp / split;
     const int sub = warp % split;
     const int leaves = kChunks / split;           // chunks owned by this warp
-    const int c0 = sub * leaves;
-    const int total_present = chunks_present(p.nv);
-    const int my_present = max(0, min(leaves, total_present - c0));
+    const int ns = (p.nv + 31) >> 5;              // strips per row
+    const int jc = (ns + kChunks - 1) / kChunks;  // strips per canonical chunk
+    const int t0 = sub * leaves * jc;             // first strip of this warp
+    const int nt = max(0, min(leaves * jc, ns - t0));
+    const int my_present = (nt + jc - 1) / jc;
+    const int total_present = (ns + jc - 1) / jc;
     const int split_present = (total_present + leaves - 1) / leaves;
-    // vectors per lane per chunk, uniform over chunks (the largest chunk)
-    const int q = p.nv / kChunks, r = p.nv % kChunks;
-    const int J = (q + (r ? 1 : 0) + 31) >> 5;
-    const int nslots = my_present * J;
+    const int vbase = t0 * 32 + lane;
+    const int R = p.ring;
+    uint4 *my_ring = dsm + static_cast<size_t>(MM) * p.nv + static_cast<size_t>(warp) * R * T * 32 + lane;
     const uint64_t pol = policy_evict_first();
 
-    uint4 wv[U];
-    bool ok[U];
-    // Issue the weight loads of slots [s0, s0 + U) of row `row`.
-    auto load_batch = [&](const uint4 *wrow, int s0) {
-        int lc = s0 / J, lj = s0 - (s0 / J) * J;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int c = c0 + lc;
-            const int v = chunk_begin(c, p.nv) + lane + 32 * lj;
-            ok[u] = (s0 + u < nslots) && (v < chunk_begin(c + 1, p.nv));
-            if (ok[u])
-                wv[u] = ld_weight_v4(wrow + v, pol);
-            if (++lj == J) { lj = 0; ++lc; }
-        }
+    auto has_row = [&](int g_) {
+        return g_ < p.groups && g_ * p.rows_per_group + row_in_group < p.N && nt > 0;
     };
-
-    // Weights are static: the first batch is requested before the wait for
-    // the previous kernel; activations are read only after it.
-    int g = blockIdx.x;
-    bool preloaded = false;
-    {
-        const int row = g * p.rows_per_group + row_in_group;
-        if (g < p.groups && row < p.N && nslots > 0) {
-            load_batch(p.W + static_cast<size_t>(row) * p.nv, 0);
-            preloaded = true;
+    // Request the K slice of group g_'s row into ring slot `slot`; always
+    // commits a group so the per-thread group count stays uniform.
+    auto issue = [&](int g_, int slot) {
+        if (has_row(g_)) {
+            const uint4 *src = p.W + static_cast<size_t>(g_ * p.rows_per_group + row_in_group) * p.nv + vbase;
+            uint4 *dst = my_ring + static_cast<size_t>(slot) * T * 32;
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                if (t < nt && vbase + 32 * t < p.nv)
+                    cp_async_16(dst + 32 * t, src + 32 * t, pol);
+            }
         }
-    }
-    pdl_wait();
-    pdl_launch_dependents();
-    for (int i = threadIdx.x; i < MM * p.nv; i += kGemvThreads)
-        xs[i] = ld_act_v4(p.x + i);
-    __syncthreads();
-
-    for (int it = 0; g < p.groups; g += gridDim.x, ++it) {
-        const int row = g * p.rows_per_group + row_in_group;
-        Acc<MM> mine;
+        cp_async_commit();
+    };
+    auto compute = [&](int slot) {
+        const uint4 *w = my_ring + static_cast<size_t>(slot) * T * 32;
+        ChunkStack<MM> stk;
+        Acc<MM> a;
 #pragma unroll
         for (int m = 0; m < MM; ++m)
-            mine.v[m] = 0.f;
-        if (row < p.N && nslots > 0) {
-            const uint4 *wrow = p.W + static_cast<size_t>(row) * p.nv;
-            ChunkStack<MM> stk;
-            Acc<MM> a;
+            a.v[m] = 0.f;
+        int cj = 0, leaf = 0;
 #pragma unroll
-            for (int m = 0; m < MM; ++m)
-                a.v[m] = 0.f;
-            int cc = 0, cj = 0;      // compute cursor: chunk (relative), j
-            for (int s0 = 0; s0 < nslots; s0 += U) {
-                if (!preloaded)
-                    load_batch(wrow, s0);
-                preloaded = false;
+        for (int t = 0; t < T; ++t) {
+            if (t < nt) {
+                const int v = vbase + 32 * t;
+                if (v < p.nv) {
+                    const uint4 wv = lds_v4(w + 32 * t);
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (s0 + u < nslots) {
-                        if (ok[u]) {
-                            const int v = chunk_begin(c0 + cc, p.nv) + lane + 32 * cj;
+                    for (int m = 0; m < MM; ++m)
+                        fma8(a.v[m], lds_v4(xs + m * p.nv + v), wv);
+                }
+                if (++cj == jc || t + 1 == nt) {
+                    // chunk complete: combine the lanes, then the tree
 #pragma unroll
-                            for (int m = 0; m < MM; ++m)
-                                fma8(a.v[m], xs[m * p.nv + v], wv[u]);
-                        }
-                        if (++cj == J) {
-                            // chunk cc complete: combine the lanes, then the tree
+                    for (int m = 0; m < MM; ++m) {
 #pragma unroll
-                            for (int m = 0; m < MM; ++m) {
-#pragma unroll
-                                for (int o = 16; o >= 1; o >>= 1)
-                                    a.v[m] += __shfl_xor_sync(0xffffffffu, a.v[m], o);
-                            }
-                            stk.push(cc, a);
-#pragma unroll
-                            for (int m = 0; m < MM; ++m)
-                                a.v[m] = 0.f;
-                            cj = 0;
-                            ++cc;
-                        }
+                        for (int o = 16; o >= 1; o >>= 1)
+                            a.v[m] += __shfl_xor_sync(0xffffffffu, a.v[m], o);
                     }
+                    stk.push(leaf++, a);
+#pragma unroll
+                    for (int m = 0; m < MM; ++m)
+                        a.v[m] = 0.f;
+                    cj = 0;
                 }
             }
-            mine = stk.flush(my_present);
         }
+        return stk.flush(my_present);
+    };
+    // Publish this warp's subtree, then combine the `split` subtrees of each
+    // row of group g_ (balanced tree) and write the outputs.
+    auto finish = [&](int it, int g_, bool mine_valid, const Acc<MM> &mine) {
         if (lane == 0) {
 #pragma unroll
             for (int m = 0; m < MM; ++m)
-                part[it & 1][warp][m] = mine.v[m];
+                part[it & 1][warp][m] = mine_valid ? mine.v[m] : 0.f;
         }
         __syncthreads();
-        // combine the `split` warp subtrees of each row: balanced tree
         const int t = threadIdx.x;
         if (t < p.rows_per_group * MM) {
             const int rr = t / MM, m = t % MM;
-            const int orow = g * p.rows_per_group + rr;
+            const int orow = g_ * p.rows_per_group + rr;
             if (orow < p.N) {
                 float v[8];
 #pragma unroll
@@ -231,43 +227,239 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p)
                 store_out(p, m, orow, v[0]);
             }
         }
+    };
+
+    // Weights are static: the first R - 1 rows are requested before the wait
+    // for the previous kernel; activations are read only after it.
+    int g = blockIdx.x;
+    for (int i = 0; i < R - 1; ++i)
+        issue(g + i * static_cast<int>(gridDim.x), i);
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i < MM * p.nv; i += kGemvThreads)
+        xs[i] = ld_act_v4(p.x + i);
+    __syncthreads();
+
+    const Acc<MM> zero = {};
+    for (int it = 0; g < p.groups; g += gridDim.x, ++it) {
+        cp_async_wait_dyn(R - 2);                 // this row's copies have landed
+        const bool v0 = has_row(g);
+        const Acc<MM> mine = v0 ? compute(it % R) : zero;
+        issue(g + (R - 1) * static_cast<int>(gridDim.x), (it + R - 1) % R);  // slot read last iteration
+        finish(it, g, v0, mine);
+    }
+    cp_async_wait<0>();                           // no copy in flight at exit
+}
+
+// Split 1: every warp owns whole rows and runs the complete canonical tree
+// itself, so the main loop has no CTA-wide barrier.  Weights are read
+// straight into registers in batches of U strips (U * 512 bytes per warp);
+// x is staged once per CTA in shared memory; the grid covers all rows
+// (rows_per_warp each) and the hardware scheduler keeps the SMs full.
+template <int MM, int U>
+__global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_kernel(const GemvParams p)
+{
+    extern __shared__ uint4 dsm[];
+    uint4 *xs = dsm;                              // [MM][nv]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ns = (p.nv + 31) >> 5;              // strips per row
+    const int jc = (ns + kChunks - 1) / kChunks;  // strips per canonical chunk
+    const int present = (ns + jc - 1) / jc;
+    const int row0 = (blockIdx.x * kWarps + warp) * p.rows_per_warp;
+    const uint64_t pol = policy_evict_first();
+
+    uint4 w[U];
+    auto load_batch = [&](const uint4 *wrow, int s0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = (s0 + u) * 32 + lane;
+            if (s0 + u < ns && v < p.nv)
+                w[u] = ld_weight_v4(wrow + v, pol);
+        }
+    };
+
+    // Weights are static: the first batch is requested before the wait for
+    // the previous kernel; activations are read only after it.
+    bool preloaded = false;
+    if (row0 < p.N) {
+        load_batch(p.W + static_cast<size_t>(row0) * p.nv, 0);
+        preloaded = true;
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i < MM * p.nv; i += kGemvThreads)
+        xs[i] = ld_act_v4(p.x + i);
+    __syncthreads();
+
+    for (int r = 0; r < p.rows_per_warp; ++r) {
+        const int row = row0 + r;
+        if (row >= p.N)
+            break;
+        const uint4 *wrow = p.W + static_cast<size_t>(row) * p.nv;
+        ChunkStack<MM> stk;
+        Acc<MM> a;
+#pragma unroll
+        for (int m = 0; m < MM; ++m)
+            a.v[m] = 0.f;
+        int cj = 0, leaf = 0;
+        for (int s0 = 0; s0 < ns; s0 += U) {
+            if (!preloaded)
+                load_batch(wrow, s0);
+            preloaded = false;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = s0 + u;
+                if (t < ns) {
+                    const int v = t * 32 + lane;
+                    if (v < p.nv) {
+#pragma unroll
+                        for (int m = 0; m < MM; ++m)
+                            fma8(a.v[m], lds_v4(xs + m * p.nv + v), w[u]);
+                    }
+                    if (++cj == jc || t + 1 == ns) {
+#pragma unroll
+                        for (int m = 0; m < MM; ++m) {
+#pragma unroll
+                            for (int o = 16; o >= 1; o >>= 1)
+                                a.v[m] += __shfl_xor_sync(0xffffffffu, a.v[m], o);
+                        }
+                        stk.push(leaf++, a);
+#pragma unroll
+                        for (int m = 0; m < MM; ++m)
+                            a.v[m] = 0.f;
+                        cj = 0;
+                    }
+                }
+            }
+        }
+        const Acc<MM> y = stk.flush(present);
+        if (lane < MM)
+            store_out(p, lane, row, lane == 0 ? y.v[0] : y.v[MM - 1]);
     }
 }
 
-} // namespace
-
-int gemv_smem_bytes(int M, int K) { return M * K * 2; }
-
-cudaError_t launch_gemv(const GemvParams &p, int grid, bool pdl, cudaStream_t s)
+template <int MM, int T>
+cudaError_t set_gemv_attr()
 {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kGemvThreads);
-    cfg.dynamicSmemBytes = gemv_smem_bytes(p.M, p.K);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    static int attr_set[2][kMaxDevices] = {};
+    static int done[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
-    int *flag = &attr_set[p.M == 1 ? 0 : 1][dev];
-    if (__atomic_load_n(flag, __ATOMIC_ACQUIRE) == 0) {
-        e = cudaFuncSetAttribute(p.M == 1 ? gemv_kernel<1, 8> : gemv_kernel<2, 8>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+    if (__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(gemv_kernel<MM, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_kernel<MM, T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+    return e;
+}
+
+template <int MM, int T>
+cudaError_t launch_t(const GemvParams &p, const cudaLaunchConfig_t &cfg)
+{
+    cudaError_t e = set_gemv_attr<MM, T>();
+    return e != cudaSuccess ? e : cudaLaunchKernelEx(&cfg, gemv_kernel<MM, T>, p);
+}
+
+template <int MM>
+cudaError_t set_rows_attr()
+{
+    static int done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(gemv_rows_kernel<MM, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_rows_kernel<MM, 8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+    return e;
+}
+
+template <int MM, int T>
+cudaError_t occupancy_t(int smem, int *ctas)
+{
+    cudaError_t e = set_gemv_attr<MM, T>();
+    return e != cudaSuccess ? e
+                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, gemv_kernel<MM, T>, kGemvThreads, smem);
+}
+
+} // namespace
+
+int gemv_smem_bytes(int M, int K, int split, int ring)
+{
+    if (split == 1)
+        return M * K * 2;   // the whole-row kernel keeps weights in registers
+    return M * K * 2 + (kGemvThreads / 32) * ring * gemv_tile_strips(K, split) * 512;
+}
+
+int gemv_tile_strips(int K, int split)
+{
+    const int n = gemv_strips_per_warp(K, split);
+    return n <= 4 ? 4 : (n <= 8 ? 8 : 16);
+}
+
+int gemv_strips_per_warp(int K, int split)
+{
+    const int ns = (K / 8 + 31) / 32;
+    const int jc = (ns + kChunks - 1) / kChunks;
+    return (kChunks / split) * jc;
+}
+
+cudaError_t gemv_occupancy(int M, int K, int split, int ring, int *ctas_per_sm)
+{
+    const int smem = gemv_smem_bytes(M, K, split, ring);
+    if (split == 1) {
+        cudaError_t e = M == 1 ? set_rows_attr<1>() : set_rows_attr<2>();
         if (e != cudaSuccess)
             return e;
-        __atomic_store_n(flag, 1, __ATOMIC_RELEASE);
+        return M == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gemv_rows_kernel<1, 8>, kGemvThreads, smem)
+                      : cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gemv_rows_kernel<2, 8>, kGemvThreads, smem);
     }
+    const int T = gemv_strips_per_warp(K, split);
+    if (M == 1)
+        return T > 8 ? occupancy_t<1, 16>(smem, ctas_per_sm)
+                     : (T > 4 ? occupancy_t<1, 8>(smem, ctas_per_sm) : occupancy_t<1, 4>(smem, ctas_per_sm));
+    return T > 8 ? occupancy_t<2, 16>(smem, ctas_per_sm)
+                 : (T > 4 ? occupancy_t<2, 8>(smem, ctas_per_sm) : occupancy_t<2, 4>(smem, ctas_per_sm));
+}
+
+cudaError_t launch_gemv(const GemvParams &p, int grid, bool pdl, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = gemv_smem_bytes(p.M, p.K, p.split, p.ring);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (p.split == 1) {
+        cudaError_t e = p.M == 1 ? set_rows_attr<1>() : set_rows_attr<2>();
+        if (e != cudaSuccess)
+            return e;
+        return p.M == 1 ? cudaLaunchKernelEx(&cfg, gemv_rows_kernel<1, 8>, p)
+                        : cudaLaunchKernelEx(&cfg, gemv_rows_kernel<2, 8>, p);
+    }
+    const int T = gemv_strips_per_warp(p.K, p.split);
+    if (T > 16 || p.ring < 2 || p.ring > 9)
+        return cudaErrorInvalidValue;
     if (p.M == 1)
-        return cudaLaunchKernelEx(&cfg, gemv_kernel<1, 8>, p);
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<2, 8>, p);
+        return T > 8 ? launch_t<1, 16>(p, cfg) : (T > 4 ? launch_t<1, 8>(p, cfg) : launch_t<1, 4>(p, cfg));
+    return T > 8 ? launch_t<2, 16>(p, cfg) : (T > 4 ? launch_t<2, 8>(p, cfg) : launch_t<2, 4>(p, cfg));
 }
 
 } // namespace skg

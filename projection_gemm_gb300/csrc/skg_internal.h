@@ -47,6 +47,8 @@ struct GemvParams {
     int split;              // warps per output row (1, 2, 4, 8)
     int rows_per_group;     // 8 / split
     int groups;             // ceil(N / rows_per_group)
+    int ring;               // weight-ring slots per warp (2..9), split > 1
+    int rows_per_warp;      // split 1: consecutive rows each warp computes
     int epilogue;           // skg_epilogue
 };
 
@@ -61,6 +63,7 @@ struct TcParams {
     int nkb;                // ceil(K / 64)
     int n_tiles;            // ceil(N / 128)
     int stages;             // shared-memory pipeline depth
+    int burst;              // k-blocks the producer requests back to back
     int epilogue;
     unsigned long long timeout_ns;
 };
@@ -73,12 +76,18 @@ constexpr unsigned kErrTimeoutDebug = 1u << 3;
 
 // Shared-memory bytes of the tensor-core kernel for (m_pad, stages).
 int tc_smem_bytes(int m_pad, int stages);
-int gemv_smem_bytes(int M, int K);
-constexpr int kGemvMaxSmem = 200 * 1024;  // x staged in shared memory: M * K * 2 bytes
+int gemv_smem_bytes(int M, int K, int split, int ring);
+int gemv_tile_strips(int K, int split);       // ring slot size in strips: 4, 8 or 16
+constexpr int kGemvMaxSmem = 226 * 1024;      // x (M * K * 2 bytes) + the weight rings (static smem needs the rest)
 int tc_max_stages(int m_pad, int smem_limit);
+int tc_tmem_cols(int m_pad);                  // TMEM columns one CTA allocates
+int tc_ctas_per_sm(int m_pad, int stages);    // co-resident CTAs (registers, shared memory, TMEM)
+constexpr int kTcDefaultStages = 4;
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_gemv(const GemvParams &p, int grid, bool pdl, cudaStream_t s);
+cudaError_t gemv_occupancy(int M, int K, int split, int ring, int *ctas_per_sm);
+int gemv_strips_per_warp(int K, int split);   // must be <= 16
 cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p,
                              int m_pad, int grid, bool pdl, cudaStream_t s);
 cudaError_t launch_prefetch_l2(const void *base, size_t bytes, cudaStream_t s);

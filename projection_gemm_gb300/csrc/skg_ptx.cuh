@@ -70,6 +70,41 @@ __device__ __forceinline__ uint4 ld_act_v4(const uint4 *p)
     return v;
 }
 
+// Asynchronous 16-byte global -> shared copy (L2 only, cache policy hint);
+// completion is tracked per thread with commit/wait groups.
+__device__ __forceinline__ void cp_async_16(void *dst_smem, const void *src, uint64_t pol)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+                 :: "r"(smem_u32(dst_smem)), "l"(src), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_dyn(int n)
+{
+    // wait_group takes an immediate: dispatch the small depths used here
+    switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+    }
+}
+
 // Bulk L2 prefetch of [p, p + bytes); bytes is a multiple of 16.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes, uint64_t pol)
 {

@@ -79,6 +79,13 @@ __device__ __forceinline__ bool epi_bar_and(bool v)
     return out != 0;
 }
 
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *ptr, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void store_out(const TcParams &p, int m, int n, float v)
 {
     const size_t idx = static_cast<size_t>(m) * p.N + n;
@@ -109,6 +116,23 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[NC])
     }
 }
 
+// acc[c] = TMEM[c] + acc[c] for NC columns, 8 at a time (keeps registers low).
+template <int NC>
+__device__ __forceinline__ void tmem_add_cols(uint32_t taddr, float (&acc)[NC])
+{
+#pragma unroll
+    for (int j = 0; j < NC / 8; ++j) {
+        uint32_t r[8];
+        tmem_ld_x8(taddr + 8 * j, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            asm volatile("" : "+r"(r[c]));
+            acc[8 * j + c] = __uint_as_float(r[c]) + acc[8 * j + c];
+        }
+    }
+}
+
 template <int NC>
 __device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)[NC])
 {
@@ -123,8 +147,54 @@ __device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)
     tmem_wait_st();
 }
 
+// The last CTA of a tile: y[m, n] for this thread's row n and columns
+// [half * NC, half * NC + NC) from the S split values in the workspace,
+// combined by the top levels of the canonical tree.  Loads are issued in
+// batches of whole columns x all S values (24 or 48 independent loads, as
+// the register budget of the CTA shape allows), so the tile costs a few L2
+// round trips instead of one per column.
+template <int S, int NC>
+__device__ __forceinline__ void reduce_tile(const TcParams &p, int n, int half, int sp)
+{
+    constexpr int kLoads = NC >= 24 ? 48 : 24;
+    constexpr int G0 = kLoads / S < 1 ? 1 : kLoads / S;
+    constexpr int G = G0 < NC ? G0 : NC;                 // columns per batch
+#pragma unroll 1
+    for (int c0 = 0; c0 < NC; c0 += G) {
+        const int mb = half * NC + c0;
+        if (mb >= p.M)
+            break;
+        float v[G][S];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int s = 0; s < S; ++s) {
+                const int m = mb + g;
+                v[g][s] = (s < sp && m < p.M)
+                              ? __ldcg(&p.ws[(static_cast<size_t>(s) * p.M + m) * p.N + n])
+                              : 0.f;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int stride = 1; stride < S; stride <<= 1) {
+#pragma unroll
+                for (int i = 0; i + stride < S; i += 2 * stride) {
+                    if (i + stride < sp)
+                        v[g][i] = v[g][i] + v[g][i + stride];
+                }
+            }
+            if (mb + g < p.M)
+                store_out(p, mb + g, n, v[g][0]);
+        }
+    }
+}
+
+// Several CTAs share an SM (a short ring each): <= 102 registers per thread
+// for m_pad 48/64 (2 CTAs per SM), <= 68 for m_pad 16/32 (3 CTAs per SM).
 template <int MPAD>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2)
 splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const TcParams p)
 {
@@ -197,18 +267,32 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             for (int i = 0; i < pre; ++i)
                 tma_load_2d(sX + i * Sh::kXBytes, &tmX, &full[i], (kb_begin + i) * kBlockK, 0, pol_x);
             int issued = pre;
-            for (int i = pre; i < nk; ++i) {
-                const int s = i % S;
-                const uint32_t ph = (i / S) & 1;
-                if (!mbar_wait(&empty[s], ph ^ 1, p.timeout_ns, &flags[0])) {
-                    record_failure(p, &flags[0], kErrTimeoutProducer);
-                    break;
+            // Steady state: wait until `burst` consecutive ring slots are free,
+            // then request their k-blocks back to back, so the bytes of each
+            // W row arrive at the memory system together.
+            const int burst = p.burst < 1 ? 1 : (p.burst > S ? S : p.burst);
+            bool ok = true;
+            for (int i = pre; i < nk && ok; i += burst) {
+                const int nb = (nk - i) < burst ? (nk - i) : burst;
+                for (int j = 0; j < nb; ++j) {
+                    const int s = (i + j) % S;
+                    const uint32_t ph = ((i + j) / S) & 1;
+                    if (!mbar_wait(&empty[s], ph ^ 1, p.timeout_ns, &flags[0])) {
+                        record_failure(p, &flags[0], kErrTimeoutProducer);
+                        ok = false;
+                        break;
+                    }
                 }
-                mbar_arrive_expect_tx(&full[s], kWBytes + Sh::kXBytes);
-                tma_load_2d(sW + s * kWBytes, &tmW, &full[s], (kb_begin + i) * kBlockK,
-                            tile * kTileN, pol_w);
-                tma_load_2d(sX + s * Sh::kXBytes, &tmX, &full[s], (kb_begin + i) * kBlockK, 0, pol_x);
-                issued = i + 1;
+                if (!ok)
+                    break;
+                for (int j = 0; j < nb; ++j) {
+                    const int s = (i + j) % S;
+                    mbar_arrive_expect_tx(&full[s], kWBytes + Sh::kXBytes);
+                    tma_load_2d(sW + s * kWBytes, &tmW, &full[s], (kb_begin + i + j) * kBlockK,
+                                tile * kTileN, pol_w);
+                    tma_load_2d(sX + s * Sh::kXBytes, &tmX, &full[s], (kb_begin + i + j) * kBlockK, 0, pol_x);
+                }
+                issued = i + nb;
             }
             if (flags[0]) {
                 // Abort: let every copy this thread issued land before exit.
@@ -276,7 +360,7 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                                    static_cast<uint32_t>(half * NC);
         const uint32_t lvl1 = lane_base + 2 * MPAD;
         const uint32_t lvl2 = lane_base + 3 * MPAD;
-        float st0[NC], cur[NC], tmp[NC];
+        float st0[NC], cur[NC];
         bool ok = true;
         for (int pl = 0; pl < present; ++pl) {
             const int b = pl & 1;
@@ -298,13 +382,9 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 #pragma unroll
                 for (int c = 0; c < NC; ++c) cur[c] = st0[c] + cur[c];
                 if (pl & 2) {
-                    tmem_load_cols<NC>(lvl1, tmp);
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) cur[c] = tmp[c] + cur[c];
+                    tmem_add_cols<NC>(lvl1, cur);
                     if (pl & 4) {
-                        tmem_load_cols<NC>(lvl2, tmp);
-#pragma unroll
-                        for (int c = 0; c < NC; ++c) cur[c] = tmp[c] + cur[c];
+                        tmem_add_cols<NC>(lvl2, cur);
                     } else {
                         tmem_store_cols<NC>(lvl2, cur);
                     }
@@ -328,15 +408,19 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                     have = true;
                 }
                 if (present & 2) {
-                    tmem_load_cols<NC>(lvl1, tmp);
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) cur[c] = have ? tmp[c] + cur[c] : tmp[c];
+                    if (have) {
+                        tmem_add_cols<NC>(lvl1, cur);
+                    } else {
+                        tmem_load_cols<NC>(lvl1, cur);
+                    }
                     have = true;
                 }
                 if (present & 4) {
-                    tmem_load_cols<NC>(lvl2, tmp);
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) cur[c] = have ? tmp[c] + cur[c] : tmp[c];
+                    if (have) {
+                        tmem_add_cols<NC>(lvl2, cur);
+                    } else {
+                        tmem_load_cols<NC>(lvl2, cur);
+                    }
                 }
             }
             if (present > 0 && n < p.N) {
@@ -347,36 +431,24 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                         p.ws[(static_cast<size_t>(split) * p.M + m) * p.N + n] = cur[c];
                 }
             }
-            __threadfence();
+            // Arrive on the tile's counter: the barrier orders every epilogue
+            // thread's partial stores before one thread's acq_rel atomic at GPU
+            // scope; the last arriver's acquire, passed on by the next
+            // barrier, orders its reads of all partials after the stores.
             epi_bar_sync();
             if (ew == 0 && lane == 0) {
-                const unsigned old = atomicAdd(&p.counters[tile], 1u);
+                const unsigned old = atom_add_acq_rel_gpu(&p.counters[tile], 1u);
                 flags[1] = (old == static_cast<unsigned>(p.split - 1)) ? 1 : 0;
             }
             epi_bar_sync();
             if (flags[1]) {
-                __threadfence();
                 const int sp = (total_present + L - 1) / L;  // splits holding a value
                 if (n < p.N) {
-#pragma unroll 1
-                    for (int c = 0; c < NC; ++c) {
-                        const int m = half * NC + c;
-                        if (m >= p.M)
-                            break;
-                        float v[kChunks];
-#pragma unroll
-                        for (int s = 0; s < kChunks; ++s)
-                            v[s] = (s < sp) ? __ldcg(&p.ws[(static_cast<size_t>(s) * p.M + m) * p.N + n])
-                                            : 0.f;
-#pragma unroll
-                        for (int stride = 1; stride < kChunks; stride <<= 1) {
-#pragma unroll
-                            for (int i2 = 0; i2 + stride < kChunks; i2 += 2 * stride) {
-                                if (i2 + stride < sp)
-                                    v[i2] = v[i2] + v[i2 + stride];
-                            }
-                        }
-                        store_out(p, m, n, v[0]);
+                    switch (p.split) {
+                    case 2: reduce_tile<2, NC>(p, n, half, sp); break;
+                    case 4: reduce_tile<4, NC>(p, n, half, sp); break;
+                    case 8: reduce_tile<8, NC>(p, n, half, sp); break;
+                    default: reduce_tile<16, NC>(p, n, half, sp); break;
                     }
                 }
                 if (ew == 0 && lane == 0)
@@ -409,6 +481,10 @@ cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcPa
         e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
         if (e != cudaSuccess)
             return e;
+        e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
         __atomic_store_n(&attr_set[dev], 232448, __ATOMIC_RELEASE);
     }
     cudaLaunchConfig_t cfg = {};
@@ -430,6 +506,24 @@ int tc_smem_bytes(int m_pad, int stages)
 {
     // 1 KB alignment slack + stages * (W tile + x tile) + barriers and flags
     return 1024 + stages * (static_cast<int>(kWBytes) + m_pad * kBlockK * 2) + 8 * (2 * stages + 5) + 16;
+}
+
+int tc_tmem_cols(int m_pad)
+{
+    int c = 32;
+    while (c < 4 * m_pad)
+        c *= 2;
+    return c;
+}
+
+int tc_ctas_per_sm(int m_pad, int stages)
+{
+    const int by_smem = 233472 / (tc_smem_bytes(m_pad, stages) + 1024);   // 228 KB per SM, 1 KB reserved per CTA
+    const int by_regs = m_pad <= 32 ? 3 : 2;                               // the kernel's launch bounds
+    const int by_tmem = 512 / tc_tmem_cols(m_pad);
+    int n = by_smem < by_regs ? by_smem : by_regs;
+    n = n < by_tmem ? n : by_tmem;
+    return n < 1 ? 1 : n;
 }
 
 int tc_max_stages(int m_pad, int smem_limit)

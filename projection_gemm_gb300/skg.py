@@ -50,6 +50,7 @@ class skg_plan_desc(ctypes.Structure):
         ("kernel_kind", ctypes.c_int), ("M", ctypes.c_int), ("N", ctypes.c_int),
         ("K", ctypes.c_int), ("epilogue", ctypes.c_int), ("split_k", ctypes.c_int),
         ("tile_n", ctypes.c_int), ("m_pad", ctypes.c_int), ("stages", ctypes.c_int),
+        ("tma_burst", ctypes.c_int),
         ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
         ("from_table", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
         ("prefetch_bytes", ctypes.c_size_t), ("pdl", ctypes.c_int),
@@ -77,7 +78,7 @@ def load(path: str = LIB_PATH):
     P = ctypes.POINTER
     lib.skg_plan_query.argtypes = [i, i, i, i, i, sz, P(skg_plan_desc)]
     lib.skg_plan.argtypes = [i, i, i, i, P(vp)]
-    lib.skg_plan_force.argtypes = [vp, i, i]
+    lib.skg_plan_force.argtypes = [vp, i, i, i, i]
     lib.skg_plan_set_pdl.argtypes = [vp, i]
     lib.skg_run.argtypes = [vp, vp, vp, vp, vp, vp]
     lib.skg_prefetch_l2.argtypes = [vp, vp, vp]
@@ -141,8 +142,8 @@ def skg_plan(M: int, N: int, K: int, epilogue) -> int:
     return h.value
 
 
-def skg_plan_force(plan: int, split_k: int = 0, stages: int = 0):
-    _check(load().skg_plan_force(plan, split_k, stages))
+def skg_plan_force(plan: int, split_k: int = 0, stages: int = 0, grid: int = 0, tma_burst: int = 0):
+    _check(load().skg_plan_force(plan, split_k, stages, grid, tma_burst))
 
 
 def skg_plan_set_pdl(plan: int, enable: bool):
@@ -190,8 +191,8 @@ class Plan:
     def info(self) -> dict:
         return skg_plan_info(self.handle)
 
-    def force(self, split_k: int = 0, stages: int = 0):
-        skg_plan_force(self.handle, split_k, stages)
+    def force(self, split_k: int = 0, stages: int = 0, grid: int = 0, tma_burst: int = 0):
+        skg_plan_force(self.handle, split_k, stages, grid, tma_burst)
 
     def set_pdl(self, enable: bool):
         skg_plan_set_pdl(self.handle, enable)

@@ -34,6 +34,23 @@ def _lib():
     assert torch.cuda.is_available()
 
 
+def force_each_split(case: DeviceCase, base, M):
+    """Run every split the plan accepts; each must reproduce `base` exactly.
+    The GEMV rejects splits whose per-warp K slice exceeds its register
+    budget (SKG_ERR_UNSUPPORTED); those are skipped."""
+    ran = []
+    for s in (GEMV_SPLITS if M <= 2 else TC_SPLITS):
+        try:
+            case.plan.force(split_k=s)
+        except skg.SkgError as e:
+            assert e.status == skg.SKG_ERR_UNSUPPORTED, e
+            continue
+        got = case.run_bits()
+        assert np.array_equal(got, base), f"split {s} changed the bits of {case.p}"
+        ran.append(s)
+    return ran
+
+
 def full_check(case: DeviceCase, y_bits, what=""):
     xb, wb, rb = case.host_bits()
     y_ref, s1, _ = O.linear(xb, wb, rb)
@@ -61,10 +78,8 @@ def test_small_shapes_all_splits(M, N, K, epi):
         assert info["kernel"] == ("gemv" if M <= 2 else "splitk_tc")
         base = case.run_bits()
         full_check(case, base, what=f"{p} default split {info['split_k']}")
-        for s in (GEMV_SPLITS if M <= 2 else TC_SPLITS):
-            case.plan.force(split_k=s)
-            got = case.run_bits()
-            assert np.array_equal(got, base), f"split {s} changed the bits of {p}"
+        ran = force_each_split(case, base, M)
+        assert len(ran) >= 2 or (M <= 2 and len(ran) >= 1), ran
     finally:
         case.close()
 
@@ -168,14 +183,12 @@ def test_chain_stages_full_size_sampled(M):
         _sampled_check(p, npts=1500)
 
 
-@pytest.mark.parametrize("M", (8, 64))
+@pytest.mark.parametrize("M", (1, 2, 8, 64))
 def test_full_size_splits_bit_identical(M):
     case = DeviceCase(sweep(M))
     try:
         base = case.run_bits()
-        for s in TC_SPLITS:
-            case.plan.force(split_k=s)
-            assert np.array_equal(case.run_bits(), base), f"split {s}"
+        assert len(force_each_split(case, base, M)) >= 2
     finally:
         case.close()
 
