@@ -206,6 +206,32 @@ SKG_API skg_status skg_plan_destroy(skg_plan_t plan);
 SKG_API skg_status skg_debug_wait_timeout(skg_plan_t plan, unsigned long long timeout_ns,
                                   void *stream);
 
+/*
+ * skg_run_noalloc -- the split-K projection (M = 3..64) for callers that may
+ * not allocate device memory: runtimes that own the whole device-memory
+ * budget, code that must not enter the CUDA allocator, or hosts that cannot
+ * create plans (skg_plan allocates).  It takes no plan, allocates nothing, and
+ * keeps the kernel's fp32 partials and arrival counters in a fixed 16 MiB
+ * array inside the library that every GPU loading the library holds until the
+ * process exits.  The pages describe no such entry point; it exists only for
+ * these callers.
+ *   M, N, K, epilogue, x, W, residual, y, stream: as for skg_plan + skg_run.
+ *   Limits: M must be 3..64 (M <= 2 needs no scratch: use skg_run); the
+ *   split's partials, split * M * N * 4 bytes, must fit 16 MiB - 64 KiB (the
+ *   split is lowered to 2 if needed, else SKG_ERR_UNSUPPORTED); N at most
+ *   16384 * 128.
+ *   The first call on each device resolves the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call clears the counters (cudaMemsetAsync on `stream`) and then
+ *   launches one kernel; results are bit-identical to skg_run's.  All calls
+ *   share the one array, so calls that overlap on the GPU (other streams, or
+ *   other threads) race: serialise them.  A bounded wait that runs out stops
+ *   the kernel but is not reported (there is no plan to hold an error word).
+ * Errors: as skg_run.
+ */
+SKG_API skg_status skg_run_noalloc(int M, int N, int K, int epilogue, const void *x, const void *W,
+                                   const void *residual, void *y, void *stream);
+
 /* Message of the last failed call on this thread ("" if none). */
 SKG_API const char *skg_last_error(void);
 

@@ -287,6 +287,85 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 } // namespace
 
+namespace skg {
+
+skg_status set_error(skg_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+skg_status prepare_splitk_launch(int M, int N, int K, int epi, const void *x, const void *W,
+                                 const void *residual, const void *y, size_t scratch_bytes,
+                                 int max_tiles, CUtensorMap *tmW, CUtensorMap *tmX, TcParams *t,
+                                 int *m_pad, int *grid)
+{
+    if (!x || !W || !y)
+        return fail(SKG_ERR_INVALID_ARG, "x, W and y must be non-NULL");
+    if (M <= 2 && M >= 1)
+        return fail(SKG_ERR_UNSUPPORTED, "M=%d runs the small-matrix kernel, which needs no scratch: use skg_run", M);
+    int dev = 0, sms = 0, l2 = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    skg_plan_desc d;
+    skg_status st = query(M, N, K, epi, sms, static_cast<size_t>(l2), &d);
+    if (st != SKG_OK)
+        return st;
+    const bool want_res = epi == SKG_EPI_BF16_RESIDUAL;
+    if (want_res != (residual != nullptr))
+        return fail(SKG_ERR_INVALID_ARG, want_res ? "this epilogue needs a residual" : "this epilogue takes no residual");
+    if (!aligned(x, 16) || !aligned(W, 16))
+        return fail(SKG_ERR_ALIGNMENT, "x and W must be 16-byte aligned");
+    if (!aligned(y, epi == SKG_EPI_FP32 ? 4 : 2) || (residual && !aligned(residual, 2)))
+        return fail(SKG_ERR_ALIGNMENT, "y / residual miss their element alignment");
+    const int n_tiles = (N + kTileN - 1) / kTileN;
+    if (n_tiles > max_tiles)
+        return fail(SKG_ERR_UNSUPPORTED, "N=%d needs %d arrival counters; the static scratch has %d", N, n_tiles,
+                    max_tiles);
+    int split = d.split_k;
+    while (split > 2 && static_cast<size_t>(split) * M * N * sizeof(float) > scratch_bytes)
+        split /= 2;
+    if (static_cast<size_t>(split) * M * N * sizeof(float) > scratch_bytes)
+        return fail(SKG_ERR_UNSUPPORTED, "M*N=%lld needs %zu bytes of partials at split 2; the static scratch holds %zu",
+                    static_cast<long long>(M) * N, static_cast<size_t>(2) * M * N * sizeof(float), scratch_bytes);
+    if (split != d.split_k)
+        fill_tc(&d, split, d.stages, d.tma_burst);
+    st = encode_2d(tmW, W, N, K, kTileN);
+    if (st != SKG_OK)
+        return st;
+    st = encode_2d(tmX, x, M, K, d.m_pad);
+    if (st != SKG_OK)
+        return st;
+    *t = TcParams{};
+    t->res = static_cast<const uint16_t *>(residual);
+    t->y = const_cast<void *>(y);
+    t->M = M;
+    t->N = N;
+    t->K = K;
+    t->split = d.split_k;
+    t->nkb = (K + kBlockK - 1) / kBlockK;
+    t->n_tiles = n_tiles;
+    t->stages = d.stages;
+    t->burst = d.tma_burst;
+    t->epilogue = epi;
+    t->timeout_ns = kDefaultTimeoutNs;
+    *m_pad = d.m_pad;
+    *grid = d.grid;
+    return SKG_OK;
+}
+
+} // namespace skg
+
 struct skg_plan_s {
     skg_plan_desc d;
     int device = 0;

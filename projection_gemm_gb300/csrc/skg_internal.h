@@ -92,6 +92,16 @@ cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, con
                              int m_pad, int grid, bool pdl, cudaStream_t s);
 cudaError_t launch_prefetch_l2(const void *base, size_t bytes, cudaStream_t s);
 cudaError_t launch_debug_wait(unsigned int *err, unsigned long long timeout_ns, cudaStream_t s);
-cudaError_t prepare_kernels();  // one-time attribute setup (max dynamic smem)
+// Records a failure message for skg_last_error and returns st.
+skg_status set_error(skg_status st, const char *fmt, ...);
+
+// Everything one split-K launch needs, worked out on the host without
+// allocating: the checks of skg_run, the launch shape the picker chooses on
+// the current device (split lowered, if needed, until the partials fit
+// scratch_bytes), and the two TMA descriptors.  ws/counters are left null.
+skg_status prepare_splitk_launch(int M, int N, int K, int epilogue, const void *x, const void *W,
+                                 const void *residual, const void *y, size_t scratch_bytes,
+                                 int max_tiles, CUtensorMap *tmW, CUtensorMap *tmX, TcParams *t,
+                                 int *m_pad, int *grid);
 
 } // namespace skg

@@ -37,6 +37,8 @@
 // own asynchronous copies / MMAs, and the CTA frees its TMEM and returns.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "skg_internal.h"
 #include "skg_ptx.cuh"
 
@@ -547,3 +549,80 @@ cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, con
 }
 
 } // namespace skg
+
+// ---------------------------------------------------------------------------
+// Scratch-free entry point.
+//
+// A caller that may not allocate device memory (a runtime that owns the
+// whole memory budget, code running where the CUDA allocator must not be
+// entered, or a host that cannot create plans because plans allocate) can
+// still run the split-K kernel: its fp32 partials and arrival counters live
+// in the fixed array below, which every GPU that loads this library holds
+// until the process exits.
+// ---------------------------------------------------------------------------
+namespace skg {
+namespace {
+
+constexpr size_t kScratchBytes = static_cast<size_t>(16) << 20;  // 16 MiB
+constexpr int kScratchTiles = 16384;                              // counters: N <= 2,097,152
+constexpr size_t kScratchCounterBytes = kScratchTiles * sizeof(unsigned int);
+
+static __device__ __align__(256) unsigned char g_splitk_scratch[kScratchBytes];
+
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_splitk_scratch on the current device, looked up once
+// per device (the host-side name is only a stand-in for the symbol).
+skg_status scratch_address(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return set_error(SKG_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev >= kMaxDevices)
+        return set_error(SKG_ERR_UNSUPPORTED, "device %d beyond %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_splitk_scratch);
+        if (e != cudaSuccess || !ptr)
+            return set_error(SKG_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_scratch_addr[dev] = ptr;
+    }
+    *out = g_scratch_addr[dev];
+    return SKG_OK;
+}
+
+} // namespace
+
+} // namespace skg
+
+extern "C" skg_status skg_run_noalloc(int M, int N, int K, int epilogue, const void *x, const void *W,
+                                      const void *residual, void *y, void *stream)
+{
+    using namespace skg;
+    void *scratch = nullptr;
+    skg_status st = scratch_address(&scratch);
+    if (st != SKG_OK)
+        return st;
+    CUtensorMap tmW, tmX;
+    TcParams t;
+    int m_pad = 0, grid = 0;
+    st = prepare_splitk_launch(M, N, K, epilogue, x, W, residual, y, kScratchBytes - kScratchCounterBytes,
+                               kScratchTiles, &tmW, &tmX, &t, &m_pad, &grid);
+    if (st != SKG_OK)
+        return st;
+    unsigned char *base = static_cast<unsigned char *>(scratch);
+    t.counters = reinterpret_cast<unsigned int *>(base);
+    t.ws = reinterpret_cast<float *>(base + kScratchCounterBytes);
+    t.err = nullptr;   // no host-visible error word: a timed-out wait only stops the kernel
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents: the counters must start at zero.
+    cudaError_t e = cudaMemsetAsync(t.counters, 0, static_cast<size_t>(t.n_tiles) * sizeof(unsigned int), s);
+    if (e == cudaSuccess)
+        e = launch_splitk_tc(tmW, tmX, t, m_pad, grid, false, s);
+    if (e != cudaSuccess)
+        return set_error(SKG_ERR_CUDA, "skg_run_noalloc launch: %s", cudaGetErrorString(e));
+    return SKG_OK;
+}

@@ -36,6 +36,7 @@ EXPORTS = (
     "skg_plan_query", "skg_plan", "skg_plan_force", "skg_plan_set_pdl", "skg_run",
     "skg_prefetch_l2", "skg_plan_set_prefetch_fraction", "skg_plan_info", "skg_plan_check",
     "skg_plan_destroy", "skg_debug_wait_timeout", "skg_last_error", "skg_version",
+    "skg_run_noalloc",
 )
 
 
@@ -87,6 +88,7 @@ def load(path: str = LIB_PATH):
     lib.skg_plan_check.argtypes = [vp]
     lib.skg_plan_destroy.argtypes = [vp]
     lib.skg_debug_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, vp]
+    lib.skg_run_noalloc.argtypes = [i, i, i, i, vp, vp, vp, vp, vp]
     for name in EXPORTS:
         getattr(lib, name).restype = ctypes.c_int
     lib.skg_last_error.restype = ctypes.c_char_p
@@ -178,6 +180,13 @@ def skg_plan_destroy(plan: int):
 
 def skg_debug_wait_timeout(plan: int, timeout_ns: int, stream=None):
     _check(load().skg_debug_wait_timeout(plan, int(timeout_ns), _stream(stream)))
+
+
+def skg_run_noalloc(M: int, N: int, K: int, epilogue, x, W, residual, y, stream=None):
+    """The split-K projection without a plan and without allocating (fixed
+    in-library scratch); see include/skg.h for its limits."""
+    _check(load().skg_run_noalloc(M, N, K, _epi(epilogue), _ptr(x), _ptr(W), _ptr(residual), _ptr(y),
+                                  _stream(stream)))
 
 
 class Plan:
