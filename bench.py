@@ -78,6 +78,30 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 of the CUDA source that defines `kernel` (its ncu counters are
+    only valid for that exact source)."""
+    import hashlib
+    src = {"splitk_tc": "skg_splitk_tc.cu", "gemv": "skg_gemv.cu"}.get(kernel)
+    if src is None:
+        return ""
+    with open(os.path.join(ROOT, "projection_gemm_gb300", "csrc", src), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu record, or None when the
+    record is missing or was taken on a different version of the kernel."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.json")
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    if rec.get("source_sha256") != kernel_source_hash(kernel):
+        return None
+    return rec.get("bytes_per_launch")
+
+
 # --------------------------------------------------------------- clock probe
 class ClockSampler:
     """nvidia-smi samples (200 ms) while the timed region runs."""
@@ -327,13 +351,7 @@ def run_ours(args):
         kk["launches"] += len(per[i])
     dom = max(kern, key=lambda k: kern[k]["us"])
     achieved = kern[dom]["bytes"] / (kern[dom]["us"] * 1e-6) / 1e9
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", f"traffic_{dom}_{args.workload}.json")
-    if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get("bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = kernel_traffic(dom, args.workload)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak_hbm, "unit": "GB/s",
                 "frac": round(achieved / peak_hbm, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
