@@ -102,6 +102,11 @@ typedef struct skg_plan_desc {
     size_t workspace_bytes; /* split-K partials + counters owned by the plan */
     size_t prefetch_bytes;  /* bytes skg_prefetch_l2 touches for this plan's W */
     int pdl;                /* 1: launched with programmatic dependent launch */
+    int l2_ahead;           /* weights requested into L2 ahead of use: TC k-blocks beyond the
+                               ring, GEMV (split 1) batches of 8 strips; 0 = none */
+    int cluster_reduce;     /* TC: 1 = the split_k CTAs of a tile form a thread-block cluster and
+                               reduce through distributed shared memory (no workspace);
+                               0 = fp32 partials in the plan's workspace, last CTA reduces */
 } skg_plan_desc;
 
 typedef struct skg_plan_s *skg_plan_t;
@@ -120,9 +125,10 @@ SKG_API skg_status skg_plan_query(int M, int N, int K, int epilogue, int num_sms
 
 /*
  * skg_plan -- build a plan for (M,N,K,epilogue) on the current CUDA device.
- * Picks the kernel as skg_plan_query does, allocates the plan's split-K
- * workspace (S*M*N fp32 partials plus one counter per 128-row tile, zeroed)
- * and a mapped host word for device-side error reports.  The plan must be
+ * Picks the kernel as skg_plan_query does and allocates a mapped host word for
+ * device-side error reports; a tensor-core plan that reduces through its
+ * global workspace (see skg_plan_set_reduction) also allocates S*M*N fp32
+ * partials plus one zeroed counter per 128-row tile.  The plan must be
  * freed with skg_plan_destroy.  One skg_run of a plan may be in flight at a
  * time (the workspace is shared); concurrent streams need separate plans.
  * Errors: as skg_plan_query, plus SKG_ERR_CUDA.  *out is NULL on failure.
@@ -178,6 +184,26 @@ SKG_API skg_status skg_run(skg_plan_t plan, const void *x, const void *W,
  * Errors: SKG_ERR_INVALID_ARG, SKG_ERR_ALIGNMENT (W_next), SKG_ERR_CUDA.
  */
 SKG_API skg_status skg_prefetch_l2(skg_plan_t next, const void *W_next, void *side_stream);
+
+/*
+ * skg_plan_set_reduction -- how the split_k CTAs of a tensor-core plan combine
+ * their partial sums: 0 (default) through the plan's global workspace and
+ * the last-arriving CTA, so every other CTA leaves as soon as it has
+ * written its partial; 1 through distributed shared memory inside a
+ * thread-block cluster (no workspace, but all S CTAs stay until the slowest
+ * arrives).  Both modes combine the partials in the same fixed order, so
+ * they give the same bits.  GEMV plans: SKG_ERR_UNSUPPORTED.
+ */
+SKG_API skg_status skg_plan_set_reduction(skg_plan_t plan, int cluster);
+
+/*
+ * skg_plan_set_l2_ahead -- [PF] applied inside a kernel: each weight tile
+ * (TC: 128 x 64 k-block; GEMV split 1: 8-strip batch of a row) is also
+ * requested into L2 `ahead` tiles before it is loaded, without using shared
+ * memory or registers.  0..16; 0 turns it off.  The GEMV ring kernel
+ * (split > 1) ignores it.
+ */
+SKG_API skg_status skg_plan_set_l2_ahead(skg_plan_t plan, int ahead);
 
 /* Fraction f in [0, 1] of the L2 that skg_prefetch_l2 fills for this plan. */
 SKG_API skg_status skg_plan_set_prefetch_fraction(skg_plan_t plan, double fraction);

@@ -44,12 +44,12 @@ skg_status cuda_fail(cudaError_t e, const char *what)
 
 // ------------------------------------------------------------ picker table
 struct TableRow {
-    int kind, M, N, K, epi, split, stages, grid, burst;
+    int kind, M, N, K, epi, split, stages, grid, burst, ahead;
 };
 
 const TableRow kTable[] = {
 #include "skg_plan_table.inc"
-    {0, 0, 0, 0, 0, 0, 0, 0, 0}  // sentinel
+    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0}  // sentinel
 };
 
 bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
@@ -121,8 +121,9 @@ void fill_tc(skg_plan_desc *d, int split, int stages, int burst)
     d->tma_burst = std::max(1, std::min(burst, d->stages));
     const int n_tiles = (d->N + kTileN - 1) / kTileN;
     d->grid = n_tiles * split;
-    d->workspace_bytes = static_cast<size_t>(split) * d->M * d->N * sizeof(float) +
-                         static_cast<size_t>(n_tiles) * sizeof(unsigned int);
+    d->workspace_bytes = d->cluster_reduce ? 0
+                                           : static_cast<size_t>(split) * d->M * d->N * sizeof(float) +
+                                                 static_cast<size_t>(n_tiles) * sizeof(unsigned int);
 }
 
 const TableRow *table_lookup(int kind, int M, int N, int K, int epi)
@@ -177,9 +178,11 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
             split = row->split;
             grid = row->grid;
             ring = row->stages;
+            d->l2_ahead = row->ahead;
             d->from_table = 1;
         } else if (N >= 4096) {
             split = 1;   // enough rows for one warp per row
+            d->l2_ahead = 1;   // measured: the next 8-strip batch into L2 while this one loads
         } else {
             // short N: warps share rows; the smallest split whose per-warp K
             // slice fits 4-strip ring slots, then finer while N is short
@@ -197,17 +200,25 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
     } else {
         int split, stages = 0, burst = 1;
         const int n_tiles = (N + kTileN - 1) / kTileN;
+        // Measured: the workspace reduction frees early CTAs' SMs for the
+        // next kernel; a cluster holds all S CTAs until the slowest arrives.
+        d->cluster_reduce = 0;
         if (row) {
             split = row->split;
             stages = row->stages;
             burst = row->burst;
+            d->l2_ahead = row->ahead;
             d->from_table = 1;
         } else {
-            // the largest split that keeps every CTA resident in one wave
+            // Measured on GB300 (back-to-back launches): about 1.5 CTAs per
+            // SM with a 4-6 stage ring streams best; deeper rings at one CTA
+            // per SM and grids beyond one wave both lose.
             const int mp = (M + 15) / 16 * 16;
-            const int slots = num_sms * tc_ctas_per_sm(mp, std::min(kTcDefaultStages, tc_max_stages(mp, 232448)));
+            stages = mp <= 16 ? 6 : (mp <= 48 ? 5 : 4);
+            stages = std::min(stages, tc_max_stages(mp, 232448));
+            const int slots = num_sms * tc_ctas_per_sm(mp, stages);
             split = 2;
-            while (split < kChunks && n_tiles * split * 2 <= slots)
+            while (split < kChunks && n_tiles * split * 2 <= std::min(slots, num_sms * 8 / 5))
                 split *= 2;
         }
         fill_tc(d, split, stages, burst);
@@ -492,6 +503,15 @@ skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out)
         delete p;
         return cuda_fail(e, "cudaHostGetDevicePointer(error word)");
     }
+    if (p->d.kernel_kind == SKG_KERNEL_SPLITK_TC && p->d.cluster_reduce) {
+        int clusters = 0;
+        e = tc_max_active_clusters(p->d.m_pad, p->d.stages, p->d.split_k, p->d.grid, &clusters);
+        if (e != cudaSuccess || clusters < 1) {
+            (void)cudaGetLastError();
+            p->d.cluster_reduce = 0;   // clusters of this size cannot be resident: reduce in memory
+            fill_tc(&p->d, p->d.split_k, p->d.stages, p->d.tma_burst);
+        }
+    }
     st = ensure_workspace(p);
     if (st != SKG_OK) {
         skg_plan_destroy(p);
@@ -568,6 +588,37 @@ skg_status skg_plan_set_pdl(skg_plan_t p, int enable)
     return SKG_OK;
 }
 
+skg_status skg_plan_set_l2_ahead(skg_plan_t p, int ahead)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_set_l2_ahead: plan is NULL");
+    if (ahead < 0 || ahead > 16)
+        return fail(SKG_ERR_INVALID_ARG, "ahead=%d outside 0..16", ahead);
+    p->d.l2_ahead = ahead;
+    return SKG_OK;
+}
+
+skg_status skg_plan_set_reduction(skg_plan_t p, int cluster)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_set_reduction: plan is NULL");
+    if (p->d.kernel_kind != SKG_KERNEL_SPLITK_TC)
+        return fail(SKG_ERR_UNSUPPORTED, "only tensor-core plans split K across CTAs");
+    skg_plan_desc d = p->d;
+    d.cluster_reduce = cluster ? 1 : 0;
+    if (d.cluster_reduce) {
+        int clusters = 0;
+        cudaError_t e = tc_max_active_clusters(d.m_pad, d.stages, d.split_k, d.grid, &clusters);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+        if (clusters < 1)
+            return fail(SKG_ERR_UNSUPPORTED, "clusters of %d CTAs cannot be resident for this plan", d.split_k);
+    }
+    fill_tc(&d, d.split_k, d.stages, d.tma_burst);
+    p->d = d;
+    return ensure_workspace(p);
+}
+
 skg_status skg_plan_set_prefetch_fraction(skg_plan_t p, double fraction)
 {
     if (!p)
@@ -625,6 +676,7 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         g.groups = (d.N + d.tile_n - 1) / d.tile_n;
         g.ring = d.stages;
         g.rows_per_warp = d.split_k == 1 ? d.tile_n / (kGemvThreads / 32) : 0;
+        g.ahead = d.l2_ahead;
         g.epilogue = d.epilogue;
         e = launch_gemv(g, d.grid, d.pdl != 0, s);
     } else {
@@ -651,6 +703,8 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         t.n_tiles = n_tiles;
         t.stages = d.stages;
         t.burst = d.tma_burst;
+        t.cluster = d.cluster_reduce ? d.split_k : 0;
+        t.ahead = d.l2_ahead;
         t.epilogue = d.epilogue;
         t.timeout_ns = kDefaultTimeoutNs;
         e = launch_splitk_tc(*mw, *mx, t, d.m_pad, d.grid, d.pdl != 0, s);

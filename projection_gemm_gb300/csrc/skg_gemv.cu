@@ -303,6 +303,16 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_kernel(const GemvPa
             a.v[m] = 0.f;
         int cj = 0, leaf = 0;
         for (int s0 = 0; s0 < ns; s0 += U) {
+            if (p.ahead > 0 && lane == 0) {
+                // the row is contiguous: ask the L2 for the batches that
+                // follow while this one is loaded into registers
+                const int a0 = s0 == 0 ? U : s0 + p.ahead * U;
+                const int a1 = min(ns, s0 + (p.ahead + 1) * U);
+                if (a0 < a1) {
+                    const int v0 = a0 * 32, v1 = min(a1 * 32, p.nv);
+                    prefetch_l2_bulk(wrow + v0, static_cast<uint32_t>((v1 - v0) * 16), pol);
+                }
+            }
             if (!preloaded)
                 load_batch(wrow, s0);
             preloaded = false;

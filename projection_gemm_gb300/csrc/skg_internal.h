@@ -48,6 +48,7 @@ struct GemvParams {
     int rows_per_group;     // 8 / split
     int groups;             // ceil(N / rows_per_group)
     int ring;               // weight-ring slots per warp (2..9), split > 1
+    int ahead;              // split 1: batches of the row requested into L2 ahead of use
     int rows_per_warp;      // split 1: consecutive rows each warp computes
     int epilogue;           // skg_epilogue
 };
@@ -64,6 +65,9 @@ struct TcParams {
     int n_tiles;            // ceil(N / 128)
     int stages;             // shared-memory pipeline depth
     int burst;              // k-blocks the producer requests back to back
+    int ahead;              // W tiles requested into L2 this many k-blocks ahead
+    int cluster;            // S: the S CTAs of a tile form a cluster and reduce
+                            // through distributed shared memory; 0: workspace
     int epilogue;
     unsigned long long timeout_ns;
 };
@@ -90,6 +94,8 @@ cudaError_t gemv_occupancy(int M, int K, int split, int ring, int *ctas_per_sm);
 int gemv_strips_per_warp(int K, int split);   // must be <= 16
 cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p,
                              int m_pad, int grid, bool pdl, cudaStream_t s);
+// Clusters of `split` CTAs the tensor-core kernel can keep resident (0 if none).
+cudaError_t tc_max_active_clusters(int m_pad, int stages, int split, int grid, int *clusters);
 cudaError_t launch_prefetch_l2(const void *base, size_t bytes, cudaStream_t s);
 cudaError_t launch_debug_wait(unsigned int *err, unsigned long long timeout_ns, cudaStream_t s);
 // Records a failure message for skg_last_error and returns st.

@@ -193,6 +193,45 @@ __device__ __forceinline__ void reduce_tile(const TcParams &p, int n, int half, 
     }
 }
 
+// Cluster mode: CTA `rank` of the tile's cluster produces rows
+// [rank * 128/S, (rank+1) * 128/S) of the tile for every column m, reading
+// the S subtree values from the S CTAs' shared memory in index order and
+// combining them by the top levels of the canonical tree (the same
+// arithmetic as the workspace reduction, so the same bits).
+template <int S, int MPAD>
+__device__ __forceinline__ void cluster_reduce(const TcParams &p, uint8_t *smem, int tile, int rank, int sp,
+                                               int et)
+{
+    constexpr int R = kTileN / S;
+    uint32_t base[S];
+    const uint32_t local = smem_u32(smem);
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+        base[s] = map_shared_rank(local, static_cast<uint32_t>(s));
+    const int items = R * p.M;
+#pragma unroll 2
+    for (int i = et; i < items; i += kEpiThreads) {
+        const int m = i / R, rr = i - (i / R) * R;   // consecutive threads: consecutive rows
+        const int row = rank * R + rr;
+        const uint32_t off = static_cast<uint32_t>((row * (MPAD + 1) + m) * 4);
+        float v[S];
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+            v[s] = (s < sp) ? ld_shared_cluster_f32(base[s] + off) : 0.f;
+#pragma unroll
+        for (int stride = 1; stride < S; stride <<= 1) {
+#pragma unroll
+            for (int j = 0; j + stride < S; j += 2 * stride) {
+                if (j + stride < sp)
+                    v[j] = v[j] + v[j + stride];
+            }
+        }
+        const int n = tile * kTileN + row;
+        if (n < p.N)
+            store_out(p, m, n, v[0]);
+    }
+}
+
 // Several CTAs share an SM (a short ring each): <= 102 registers per thread
 // for m_pad 48/64 (2 CTAs per SM), <= 68 for m_pad 16/32 (3 CTAs per SM).
 template <int MPAD>
@@ -219,8 +258,9 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort, [1] last
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x % p.n_tiles;
-    const int split = blockIdx.x / p.n_tiles;
+    // cluster mode: the S CTAs of a tile are consecutive (one cluster)
+    const int tile = p.cluster ? blockIdx.x / p.split : blockIdx.x % p.n_tiles;
+    const int split = p.cluster ? blockIdx.x % p.split : blockIdx.x / p.n_tiles;
     const int L = kChunks / p.split;
     const int leaf0 = split * L;
     const int total_present = chunks_present(p.nkb);
@@ -260,6 +300,10 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
             const int pre = nk < S ? nk : S;
+            // W tiles beyond the ring are requested into L2 `ahead` k-blocks
+            // in advance (weights only: allowed before the wait below)
+            for (int i = pre; i < nk && i < pre + p.ahead; ++i)
+                tma_prefetch_l2_2d(&tmW, (kb_begin + i) * kBlockK, tile * kTileN);
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full[i], kWBytes + Sh::kXBytes);
                 tma_load_2d(sW + i * kWBytes, &tmW, &full[i], (kb_begin + i) * kBlockK,
@@ -289,6 +333,8 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                     break;
                 for (int j = 0; j < nb; ++j) {
                     const int s = (i + j) % S;
+                    if (p.ahead > 0 && i + j + p.ahead < nk)
+                        tma_prefetch_l2_2d(&tmW, (kb_begin + i + j + p.ahead) * kBlockK, tile * kTileN);
                     mbar_arrive_expect_tx(&full[s], kWBytes + Sh::kXBytes);
                     tma_load_2d(sW + s * kWBytes, &tmW, &full[s], (kb_begin + i + j) * kBlockK,
                                 tile * kTileN, pol_w);
@@ -425,6 +471,17 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                     }
                 }
             }
+            if (p.cluster) {
+                // this CTA's subtree into its own (now idle) ring memory,
+                // rows of m_pad + 1 floats so both access patterns are
+                // free of bank conflicts
+                if (present > 0) {
+                    float *part = reinterpret_cast<float *>(smem);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c)
+                        part[row * (MPAD + 1) + half * NC + c] = cur[c];
+                }
+            } else {
             if (present > 0 && n < p.N) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
@@ -456,7 +513,26 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 if (ew == 0 && lane == 0)
                     p.counters[tile] = 0;
             }
+            }   // workspace mode
         }
+    }
+
+    if (p.cluster) {
+        // Every thread of every CTA of the cluster passes both barriers on
+        // every path (a skipped arrival would stall the peers).
+        __syncwarp();
+        cluster_sync();   // all partials written and visible
+        if (warp >= 2) {
+            const int sp = (total_present + L - 1) / L;
+            switch (p.split) {
+            case 2: cluster_reduce<2, MPAD>(p, smem, tile, split, sp, threadIdx.x - 64); break;
+            case 4: cluster_reduce<4, MPAD>(p, smem, tile, split, sp, threadIdx.x - 64); break;
+            case 8: cluster_reduce<8, MPAD>(p, smem, tile, split, sp, threadIdx.x - 64); break;
+            default: cluster_reduce<16, MPAD>(p, smem, tile, split, sp, threadIdx.x - 64); break;
+            }
+        }
+        __syncwarp();
+        cluster_sync();   // no CTA leaves while a peer still reads its memory
     }
 
     tc_fence_before();
@@ -487,6 +563,9 @@ cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcPa
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
+        e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess)
+            return e;
         __atomic_store_n(&attr_set[dev], 232448, __ATOMIC_RELEASE);
     }
     cudaLaunchConfig_t cfg = {};
@@ -494,11 +573,22 @@ cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcPa
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (p.cluster) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, splitk_tc_kernel<MPAD>, tmW, tmX, p);
 }
 
@@ -534,6 +624,50 @@ int tc_max_stages(int m_pad, int smem_limit)
     while (s > 2 && tc_smem_bytes(m_pad, s) > smem_limit)
         --s;
     return s;
+}
+
+template <int MPAD>
+cudaError_t max_clusters_t(int stages, int split, int grid, int *clusters)
+{
+    // the attributes the launch sets (shared memory, cluster size) first
+    static int done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess)
+            return e;
+        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = tc_smem_bytes(MPAD, stages);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, splitk_tc_kernel<MPAD>, &cfg);
+}
+
+cudaError_t tc_max_active_clusters(int m_pad, int stages, int split, int grid, int *clusters)
+{
+    switch (m_pad) {
+    case 16: return max_clusters_t<16>(stages, split, grid, clusters);
+    case 32: return max_clusters_t<32>(stages, split, grid, clusters);
+    case 48: return max_clusters_t<48>(stages, split, grid, clusters);
+    case 64: return max_clusters_t<64>(stages, split, grid, clusters);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p,

@@ -36,7 +36,7 @@ EXPORTS = (
     "skg_plan_query", "skg_plan", "skg_plan_force", "skg_plan_set_pdl", "skg_run",
     "skg_prefetch_l2", "skg_plan_set_prefetch_fraction", "skg_plan_info", "skg_plan_check",
     "skg_plan_destroy", "skg_debug_wait_timeout", "skg_last_error", "skg_version",
-    "skg_run_noalloc",
+    "skg_run_noalloc", "skg_plan_set_reduction", "skg_plan_set_l2_ahead",
 )
 
 
@@ -54,7 +54,8 @@ class skg_plan_desc(ctypes.Structure):
         ("tma_burst", ctypes.c_int),
         ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
         ("from_table", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
-        ("prefetch_bytes", ctypes.c_size_t), ("pdl", ctypes.c_int),
+        ("prefetch_bytes", ctypes.c_size_t), ("pdl", ctypes.c_int), ("l2_ahead", ctypes.c_int),
+        ("cluster_reduce", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -89,6 +90,8 @@ def load(path: str = LIB_PATH):
     lib.skg_plan_destroy.argtypes = [vp]
     lib.skg_debug_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, vp]
     lib.skg_run_noalloc.argtypes = [i, i, i, i, vp, vp, vp, vp, vp]
+    lib.skg_plan_set_reduction.argtypes = [vp, i]
+    lib.skg_plan_set_l2_ahead.argtypes = [vp, i]
     for name in EXPORTS:
         getattr(lib, name).restype = ctypes.c_int
     lib.skg_last_error.restype = ctypes.c_char_p
@@ -152,6 +155,14 @@ def skg_plan_set_pdl(plan: int, enable: bool):
     _check(load().skg_plan_set_pdl(plan, 1 if enable else 0))
 
 
+def skg_plan_set_l2_ahead(plan: int, ahead: int):
+    _check(load().skg_plan_set_l2_ahead(plan, int(ahead)))
+
+
+def skg_plan_set_reduction(plan: int, cluster: bool):
+    _check(load().skg_plan_set_reduction(plan, 1 if cluster else 0))
+
+
 def skg_plan_set_prefetch_fraction(plan: int, fraction: float):
     _check(load().skg_plan_set_prefetch_fraction(plan, float(fraction)))
 
@@ -205,6 +216,12 @@ class Plan:
 
     def set_pdl(self, enable: bool):
         skg_plan_set_pdl(self.handle, enable)
+
+    def set_l2_ahead(self, ahead: int):
+        skg_plan_set_l2_ahead(self.handle, ahead)
+
+    def set_reduction(self, cluster: bool):
+        skg_plan_set_reduction(self.handle, cluster)
 
     def run(self, x, W, residual, y, stream=None):
         skg_run(self.handle, x, W, residual, y, stream)

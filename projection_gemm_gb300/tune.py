@@ -1,0 +1,150 @@
+"""Fill the picker table from timings taken on the GPU.
+
+For every projection shape of the workloads (the batch sweep, the wide and
+deep-K projections and the five decode-layer chain stages) and every M they
+are run at, each candidate launch configuration inside the kernel kind that
+M selects is timed back to back -- the way a decode step issues projections
+-- over enough distinct copies of the weight that no launch finds its weight
+in L2.  The fastest candidate becomes a row of csrc/skg_plan_table.inc; the
+full log is written as JSON beside it.
+
+usage: python -m projection_gemm_gb300.tune [--out-inc PATH] [--out-log PATH] [--rounds R]
+Rebuild the library afterwards (the table is compiled in).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import time
+
+import torch
+
+from . import build, skg
+from .inputs import CHAIN_M, CHAIN_STAGES, DEEPK_M, SWEEP_M, WIDE_M, Projection, generate
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+NOMINAL_HBM_BPS = 8.0e12   # no launch can stream its weight faster than the HBM
+INC = os.path.join(HERE, "csrc", "skg_plan_table.inc")
+
+
+def shapes():
+    """(N, K, epilogue) -> the M values it runs at."""
+    out = {}
+    def add(N, K, epi, ms):
+        out.setdefault((N, K, epi), set()).update(ms)
+    add(7168, 7168, "bf16", SWEEP_M)
+    add(12288, 7168, "bf16", WIDE_M)
+    add(7168, 16384, "bf16_residual", DEEPK_M)
+    for K, N, epi in CHAIN_STAGES:
+        add(N, K, epi, CHAIN_M)
+    return {k: sorted(v) for k, v in out.items()}
+
+
+def candidates(M, N, K):
+    if M <= 2:
+        c = [{"split_k": 1, "ahead": a} for a in (0, 1, 2)]
+        for split in (2, 4, 8):
+            for ring in (2, 3, 4):
+                c.append({"split_k": split, "stages": ring, "ahead": 0})
+        return c
+    return [{"split_k": s, "stages": st, "ahead": 0} for s in (2, 4, 8, 16) for st in (3, 4, 5, 6)]
+
+
+def time_config(M, N, K, epi, cfg, Ws, x, res, y, rounds):
+    """Launch time per projection: one round over every weight copy is
+    captured in a CUDA graph and replayed `rounds` times (no host launch
+    cost in the measurement; programmatic dependent launch stays on)."""
+    p = None
+    try:
+        p = skg.Plan(M, N, K, epi)
+        force = {k: v for k, v in cfg.items() if k in ("split_k", "stages") and v}
+        p.force(**force)
+        p.set_l2_ahead(cfg.get("ahead", 0))
+        for W in Ws[:2]:
+            p.run(x, W, res, y)             # descriptors, attributes: outside the capture
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for W in Ws:
+                p.run(x, W, res, y, s)
+        # replay() launches on the current stream: time on that stream
+        g.replay()
+        torch.cuda.synchronize()
+        main = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(main)
+        for _ in range(rounds):
+            g.replay()
+        b.record(main)
+        torch.cuda.synchronize()
+        p.check()
+        us = a.elapsed_time(b) * 1e3 / (rounds * len(Ws))
+        if 2 * N * K / (us * 1e-6) > NOMINAL_HBM_BPS:
+            raise RuntimeError(f"implausible timing {us:.3f} us for {2 * N * K} weight bytes")
+        return us, p.info()
+    except skg.SkgError:
+        return None, None
+    finally:
+        if p is not None:
+            p.close()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out-inc", default=INC)
+    ap.add_argument("--out-log", default=None)
+    ap.add_argument("--rounds", type=int, default=40)
+    args = ap.parse_args(argv)
+    build.build()
+    skg.load()
+    torch.cuda.set_device(0)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    rows, log = [], []
+    t0 = time.time()
+    for (N, K, epi), ms in shapes().items():
+        wbytes = 2 * N * K
+        copies = max(7, math.ceil(3 * l2 / wbytes))
+        base = generate(Projection(64, N, K, epi, seed=900)).W.cuda()
+        Ws = [base.roll(i, dims=0).contiguous() for i in range(copies)]   # distinct bytes, same statistics
+        del base
+        for M in ms:
+            t = generate(Projection(M, N, K, epi, seed=901 + M))
+            x = t.x.cuda()
+            res = None if t.res is None else t.res.cuda()
+            y = torch.empty(M, N, dtype=torch.float32 if epi == "fp32" else torch.bfloat16, device="cuda")
+            results = []
+            for cfg in candidates(M, N, K):
+                us, info = time_config(M, N, K, epi, cfg, Ws, x, res, y, args.rounds)
+                if us is not None:
+                    results.append((us, cfg, info))
+                    log.append({"M": M, "N": N, "K": K, "epilogue": epi, "config": cfg, "us": round(us, 3),
+                                "weight_gbs": round(wbytes / us / 1e3, 1)})
+            us, cfg, info = min(results, key=lambda r: r[0])
+            kind = info["kernel_kind"]
+            rows.append((kind, M, N, K, skg.EPILOGUES[epi], info["split_k"],
+                         info["stages"] if kind == skg.SKG_KERNEL_SPLITK_TC or info["split_k"] > 1 else 0,
+                         0, 1, cfg.get("ahead", 0), us, wbytes / us / 1e3))
+            print(f"N={N} K={K} {epi} M={M}: best {cfg} {us:.2f} us {wbytes / us / 1e3:.0f} GB/s", flush=True)
+        del Ws
+        torch.cuda.empty_cache()
+    with open(args.out_inc, "w") as f:
+        f.write("// skg_plan_table.inc -- measured picker table.\n//\n"
+                "// Each row: { kernel_kind, M, N, K, epilogue, split_k, stages, grid, tma_burst, l2_ahead }.\n"
+                "// stages: TC ring stages / GEMV weight-ring slots (0 = library default);\n"
+                "// grid = 0 lets the library size the grid.  Written by projection_gemm_gb300/tune.py\n"
+                f"// from back-to-back timings on {torch.cuda.get_device_name(0)} "
+                f"({len(rows)} rows, {time.time() - t0:.0f} s); the comment on each row is the\n"
+                "// measured time per launch and weight-stream rate.\n")
+        for r in rows:
+            f.write("{%d, %d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.2f us, %.0f GB/s\n" % r)
+    if args.out_log:
+        with open(args.out_log, "w") as f:
+            json.dump(log, f, indent=0)
+    print(f"wrote {args.out_inc} ({len(rows)} rows)")
+
+
+if __name__ == "__main__":
+    main()

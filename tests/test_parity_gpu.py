@@ -47,6 +47,13 @@ def force_each_split(case: DeviceCase, base, M):
             continue
         got = case.run_bits()
         assert np.array_equal(got, base), f"split {s} changed the bits of {case.p}"
+        if M > 2:
+            # the same split reduced through the global workspace instead of
+            # the cluster's shared memory: same order, same bits
+            cluster = case.plan.info()["cluster_reduce"]
+            case.plan.set_reduction(not cluster)
+            assert np.array_equal(case.run_bits(), base), f"split {s} reduction mode changed the bits"
+            case.plan.set_reduction(cluster)
         ran.append(s)
     return ran
 
