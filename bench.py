@@ -92,7 +92,7 @@ def kernel_source_hash(kernel: str) -> str:
 def kernel_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu record, or None when the
     record is missing or was taken on a different version of the kernel."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.json")
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
     try:
         rec = json.load(open(path))
     except Exception:
