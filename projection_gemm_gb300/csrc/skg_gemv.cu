@@ -348,6 +348,92 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_kernel(const GemvPa
     }
 }
 
+// Whole rows per warp, specialised for K % 256 == 0 (every strip full):
+// JC strips per canonical chunk is a compile-time constant, a batch is
+// 8 strips = 8/JC whole chunks, and bounds are checked per chunk only.  Same
+// arithmetic, same order as gemv_rows_kernel.  (Staging x as fp32 instead of
+// bf16 measured slower: it doubles the shared-memory bytes read per weight.)
+template <int MM, int JC>
+__global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_fast_kernel(const GemvParams p)
+{
+    constexpr int U = 8;                          // strips per batch
+    constexpr int B = U / JC;                     // chunks per batch
+    extern __shared__ uint4 dsm[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nch = (p.nv >> 5) / JC;             // present chunks (<= 16)
+    const int row0 = (blockIdx.x * kWarps + warp) * p.rows_per_warp;
+    const uint64_t pol = policy_evict_first();
+
+    uint4 w[U];
+    auto load_batch = [&](const uint4 *wrow, int c0) {
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            if (c0 + b < nch) {
+#pragma unroll
+                for (int j = 0; j < JC; ++j)
+                    w[b * JC + j] = ld_weight_v4(wrow + ((c0 + b) * JC + j) * 32 + lane, pol);
+            }
+        }
+    };
+
+    bool preloaded = false;
+    if (row0 < p.N) {
+        load_batch(p.W + static_cast<size_t>(row0) * p.nv, 0);
+        preloaded = true;
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i < MM * p.nv; i += kGemvThreads)
+        dsm[i] = ld_act_v4(p.x + i);
+    __syncthreads();
+
+    for (int r = 0; r < p.rows_per_warp; ++r) {
+        const int row = row0 + r;
+        if (row >= p.N)
+            break;
+        const uint4 *wrow = p.W + static_cast<size_t>(row) * p.nv;
+        ChunkStack<MM> stk;
+        for (int c0 = 0; c0 < nch; c0 += B) {
+            if (p.ahead > 0 && lane == 0) {
+                const int a0 = (c0 == 0 ? B : c0 + p.ahead * B) * JC * 32;
+                const int a1 = min(nch, c0 + (p.ahead + 1) * B) * JC * 32;
+                if (a0 < a1)
+                    prefetch_l2_bulk(wrow + a0, static_cast<uint32_t>((a1 - a0) * 16), pol);
+            }
+            if (!preloaded)
+                load_batch(wrow, c0);
+            preloaded = false;
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                if (c0 + b < nch) {
+                    Acc<MM> a;
+#pragma unroll
+                    for (int m = 0; m < MM; ++m)
+                        a.v[m] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < JC; ++j) {
+                        const int v = ((c0 + b) * JC + j) * 32 + lane;
+                        const uint4 wv = w[b * JC + j];
+#pragma unroll
+                        for (int m = 0; m < MM; ++m)
+                            fma8(a.v[m], lds_v4(dsm + m * p.nv + v), wv);
+                    }
+#pragma unroll
+                    for (int m = 0; m < MM; ++m) {
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1)
+                            a.v[m] += __shfl_xor_sync(0xffffffffu, a.v[m], o);
+                    }
+                    stk.push(c0 + b, a);
+                }
+            }
+        }
+        const Acc<MM> y = stk.flush(nch);
+        if (lane < MM)
+            store_out(p, lane, row, lane == 0 ? y.v[0] : y.v[MM - 1]);
+    }
+}
+
 template <int MM, int T>
 cudaError_t set_gemv_attr()
 {
@@ -397,6 +483,46 @@ cudaError_t set_rows_attr()
     return e;
 }
 
+template <int MM, int JC>
+cudaError_t set_fast_attr()
+{
+    static int done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(gemv_rows_fast_kernel<MM, JC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kGemvMaxSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_rows_fast_kernel<MM, JC>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+    return e;
+}
+
+template <int MM, int JC>
+cudaError_t launch_fast_t(const GemvParams &p, const cudaLaunchConfig_t &cfg)
+{
+    cudaError_t e = set_fast_attr<MM, JC>();
+    return e != cudaSuccess ? e : cudaLaunchKernelEx(&cfg, gemv_rows_fast_kernel<MM, JC>, p);
+}
+
+template <int MM>
+cudaError_t launch_fast_jc(const GemvParams &p, const cudaLaunchConfig_t &cfg, int jc)
+{
+    switch (jc) {
+    case 1: return launch_fast_t<MM, 1>(p, cfg);
+    case 2: return launch_fast_t<MM, 2>(p, cfg);
+    case 4: return launch_fast_t<MM, 4>(p, cfg);
+    default: return launch_fast_t<MM, 8>(p, cfg);
+    }
+}
+
 template <int MM, int T>
 cudaError_t occupancy_t(int smem, int *ctas)
 {
@@ -407,10 +533,23 @@ cudaError_t occupancy_t(int smem, int *ctas)
 
 } // namespace
 
+// Strips per canonical chunk when every strip is full (K % 256 == 0) and the
+// whole-row kernel can take it at compile time; 0 otherwise.
+int gemv_fast_jc(int K)
+{
+    if (K % 256 != 0)
+        return 0;
+    const int ns = K / 256;
+    const int jc = (ns + kChunks - 1) / kChunks;
+    if (ns % jc != 0)
+        return 0;
+    return (jc == 1 || jc == 2 || jc == 4 || jc == 8) ? jc : 0;
+}
+
 int gemv_smem_bytes(int M, int K, int split, int ring)
 {
-    if (split == 1)
-        return M * K * 2;   // the whole-row kernel keeps weights in registers
+    if (split == 1)   // the whole-row kernels keep weights in registers; x in shared memory
+        return M * K * 2;
     return M * K * 2 + (kGemvThreads / 32) * ring * gemv_tile_strips(K, split) * 512;
 }
 
@@ -457,6 +596,9 @@ cudaError_t launch_gemv(const GemvParams &p, int grid, bool pdl, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    const int jc = gemv_fast_jc(p.K);
+    if (p.split == 1 && jc > 0)
+        return p.M == 1 ? launch_fast_jc<1>(p, cfg, jc) : launch_fast_jc<2>(p, cfg, jc);
     if (p.split == 1) {
         cudaError_t e = p.M == 1 ? set_rows_attr<1>() : set_rows_attr<2>();
         if (e != cudaSuccess)

@@ -82,6 +82,7 @@ constexpr unsigned kErrTimeoutDebug = 1u << 3;
 int tc_smem_bytes(int m_pad, int stages);
 int gemv_smem_bytes(int M, int K, int split, int ring);
 int gemv_tile_strips(int K, int split);       // ring slot size in strips: 4, 8 or 16
+int gemv_fast_jc(int K);                      // >0: the specialised whole-row kernel applies
 constexpr int kGemvMaxSmem = 226 * 1024;      // x (M * K * 2 bytes) + the weight rings (static smem needs the rest)
 int tc_max_stages(int m_pad, int smem_limit);
 int tc_tmem_cols(int m_pad);                  // TMEM columns one CTA allocates
