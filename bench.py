@@ -11,7 +11,7 @@ one batch of synthetic inputs:
                    719 MB of weights and no weight is L2-resident when its
                    projection runs (inputs larger than the 126 MB L2).
   chain            the five projections of a decode layer at M = 1, 8, 64,
-                   the next weight prefetched into L2 on a side stream.
+                   each launch asking the L2 for the start of the next weight.
   wide / deepk     the wide input projection and the deep-K output projection
                    with residual, at their M values.
 
@@ -60,8 +60,8 @@ def workload(name: str):
     if name == "chain":
         projs = [p for m in I.CHAIN_M for p in I.chain(m)]
         return projs, ("decode-layer chain at M in {1,8,64}: 7168->12288, 8192->7168 (+res), "
-                       "7168->384 (fp32), 7168->4096, 4096->7168 (+res); next W prefetched to L2 "
-                       "on a side stream"), {"M": list(I.CHAIN_M), "stages": [list(s) for s in I.CHAIN_STAGES]}
+                       "7168->384 (fp32), 7168->4096, 4096->7168 (+res); each launch asks the L2 "
+                       "for the start of the next W"), {"M": list(I.CHAIN_M), "stages": [list(s) for s in I.CHAIN_STAGES]}
     if name == "pr1":
         return [I.pr1()], "PR1: M=1, K=N=1024, + residual", {"M": [1], "N": 1024, "K": 1024,
                                                               "epilogue": "bf16_residual"}
@@ -249,46 +249,87 @@ def run_ours(args):
     projs, desc, cfg = workload(args.workload)
     peak_hbm, peak_tf, peak_src = load_peaks()
 
-    # operands resident in HBM
+    # Operands resident in HBM.  A step's activations (x, residual) and its
+    # outputs each live in one packed buffer (256-byte aligned segments), so
+    # the end-to-end run moves them with one host->device and one
+    # device->host copy per step.
+    def seg(nbytes):
+        return (nbytes + 255) // 256 * 256
+    gens = [generate(p) for p in projs]
+    in_bytes = sum(seg(t.x.numel() * 2) + (seg(t.res.numel() * 2) if t.res is not None else 0) for t in gens)
+    out_bytes = sum(seg(p.M * p.N * p.out_bytes_per_elem) for p in projs)
+    dev_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    dev_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+    host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    host_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+
+    def view(buf, off, shape, dt):
+        n = shape[0] * shape[1] * torch.empty((), dtype=dt).element_size()
+        return buf[off:off + n].view(dt).view(*shape)
+
     ops, hostcopy = [], []
-    for p in projs:
-        t = generate(p)
+    oi = oo = 0
+    for p, t in zip(projs, gens):
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             from projection_gemm_gb300.inputs import bits
             hostcopy.append((p, bits(t.x), bits(t.W), None if t.res is None else bits(t.res)))
         plan = skg.Plan(p.M, p.N, p.K, p.epilogue)
         plan.set_pdl(bool(args.pdl))
         dt = torch.float32 if p.epilogue == "fp32" else torch.bfloat16
-        ops.append(dict(p=p, plan=plan, info=plan.info(),
-                        x=t.x.to(dev), W=t.W.to(dev),
-                        res=None if t.res is None else t.res.to(dev),
-                        y=torch.empty(p.M, p.N, dtype=dt, device=dev),
-                        hx=t.x.pin_memory(), hres=None if t.res is None else t.res.pin_memory(),
-                        hy=torch.empty(p.M, p.N, dtype=dt).pin_memory()))
-        del t
-    # [PF] the next projection's weight is prefetched into L2 on a side stream
-    # while the current one runs (default: the chain; any workload with --prefetch)
-    chain = args.workload == "chain" if args.prefetch is None else args.prefetch > 0
+        x = view(dev_in, oi, (p.M, p.K), torch.bfloat16)
+        view(host_in, oi, (p.M, p.K), torch.bfloat16).copy_(t.x)
+        oi += seg(t.x.numel() * 2)
+        res = None
+        if t.res is not None:
+            res = view(dev_in, oi, (p.M, p.N), torch.bfloat16)
+            view(host_in, oi, (p.M, p.N), torch.bfloat16).copy_(t.res)
+            oi += seg(t.res.numel() * 2)
+        y = view(dev_out, oo, (p.M, p.N), dt)
+        oo += seg(p.M * p.N * p.out_bytes_per_elem)
+        ops.append(dict(p=p, plan=plan, info=plan.info(), x=x, W=t.W.to(dev), res=res, y=y))
+    dev_in.copy_(host_in)
+    del gens
+    # [PF] on a side stream (--prefetch f): a prefetch kernel fills the L2
+    # with the next projection's weight while the current one runs.
+    side_pf = args.prefetch is not None and args.prefetch > 0
     side = torch.cuda.Stream(device=dev)
     stream = torch.cuda.current_stream(dev)
     if args.prefetch is not None:
         for o in ops:
             skg.skg_plan_set_prefetch_fraction(o["plan"].handle, max(0.0, args.prefetch))
 
-    def step(events=None):
+    # [PF] inside the launch: each projection also asks the L2 for the first
+    # part of the weight that runs after it (the step wraps around).
+    next_frac = args.next_weight if args.next_weight is not None else (0.15 if args.workload == "chain" else 0.0)
+    if next_frac > 0:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         for i, o in enumerate(ops):
-            if chain and i + 1 < len(ops) and ops[i + 1]["info"]["prefetch_bytes"] > 0:
+            nxt = ops[(i + 1) % len(ops)]
+            o["plan"].set_next_weight(nxt["W"], int(min(nxt["p"].weight_bytes(), next_frac * l2)))
+
+    # Runs of consecutive launches of one kernel kind: events at their
+    # boundaries time each kind's launches without splitting the runs.
+    groups, g0 = [], 0
+    for i in range(1, len(ops) + 1):
+        if i == len(ops) or ops[i]["info"]["kernel"] != ops[g0]["info"]["kernel"]:
+            groups.append((g0, i))
+            g0 = i
+    group_start = {a: j for j, (a, _) in enumerate(groups)}
+
+    def step(events=None, mode="launch"):
+        for i, o in enumerate(ops):
+            if side_pf and i + 1 < len(ops) and ops[i + 1]["info"]["prefetch_bytes"] > 0:
                 side.wait_stream(stream)
                 ops[i + 1]["plan"].prefetch(ops[i + 1]["W"], side)
-            if events is not None:
-                events[i].record(stream)
+            if events is not None and (mode == "launch" or i in group_start):
+                events[i if mode == "launch" else group_start[i]].record(stream)
             o["plan"].run(o["x"], o["W"], o["res"], o["y"], stream)
-            if chain and i + 1 < len(ops):
+            if side_pf and i + 1 < len(ops):
                 stream.wait_stream(side)
         if events is not None:
-            events[len(ops)].record(stream)
+            events[-1].record(stream)
 
-    launches_per_step = len(ops) + (sum(1 for o in ops[1:] if o["info"]["prefetch_bytes"] > 0) if chain else 0)
+    launches_per_step = len(ops) + (sum(1 for o in ops[1:] if o["info"]["prefetch_bytes"] > 0) if side_pf else 0)
     wbytes_step = sum(o["p"].weight_bytes() for o in ops)
 
     warm = max(3, args.warmup)
@@ -299,9 +340,16 @@ def run_ours(args):
     torch.cuda.synchronize()
     est = (time.perf_counter() - t0) / warm
     K = args.steps if args.steps else max(20, min(40000, int(args.seconds / max(est, 1e-6))))
+    # Sampled steps carry events, alternately before every launch (the
+    # us/projection figures) or at kernel-kind boundaries only (each kind's
+    # launch durations, with the programmatic overlap inside a run intact).
+    # An event between two launches ends their overlap, so only about 300 of
+    # the K steps carry any.
     sample_every = max(1, K // 300)
     sampled = list(range(0, K, sample_every))
-    evs = {k: [torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for k in sampled}
+    modes = {k: ("launch" if j % 2 == 0 else "group") for j, k in enumerate(sampled)}
+    evs = {k: [torch.cuda.Event(enable_timing=True)
+               for _ in range((len(ops) if modes[k] == "launch" else len(groups)) + 1)] for k in sampled}
 
     clocks = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
         if not args.no_clocks else None
@@ -316,7 +364,7 @@ def run_ours(args):
     w0 = time.time()
     start.record(stream)
     for k in range(K):
-        step(evs.get(k))
+        step(evs.get(k), modes.get(k, "launch"))
     end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
@@ -332,11 +380,19 @@ def run_ours(args):
 
     # per-launch durations from the sampled steps (events on the launch stream)
     per = {i: [] for i in range(len(ops))}
+    kern = {}
     for k in sampled:
         e = evs[k]
-        for i in range(len(ops)):
-            per[i].append(e[i].elapsed_time(e[i + 1]) * 1e3)  # us
-    per_m, kern = {}, {}
+        if modes[k] == "launch":
+            for i in range(len(ops)):
+                per[i].append(e[i].elapsed_time(e[i + 1]) * 1e3)  # us
+            continue
+        for j, (a, b) in enumerate(groups):
+            kk = kern.setdefault(ops[a]["info"]["kernel"], {"bytes": 0.0, "us": 0.0, "launches": 0})
+            kk["bytes"] += sum(ops[i]["p"].algorithmic_bytes() for i in range(a, b))
+            kk["us"] += e[j].elapsed_time(e[j + 1]) * 1e3
+            kk["launches"] += b - a
+    per_m = {}
     for i, o in enumerate(ops):
         p = o["p"]
         us = statistics.median(per[i])
@@ -345,17 +401,14 @@ def run_ours(args):
         per_m[key] = {"M": p.M, "N": p.N, "K": p.K, "kernel": o["info"]["kernel"], "split": o["info"]["split_k"],
                       "us": round(us, 3), "weight_gbs": round(p.weight_bytes() / us / 1e3, 1),
                       "roofline_frac": round(t_ideal / us, 4)}
-        kk = kern.setdefault(o["info"]["kernel"], {"bytes": 0.0, "us": 0.0, "launches": 0})
-        kk["bytes"] += p.algorithmic_bytes() * len(per[i])
-        kk["us"] += sum(per[i])
-        kk["launches"] += len(per[i])
     dom = max(kern, key=lambda k: kern[k]["us"])
     achieved = kern[dom]["bytes"] / (kern[dom]["us"] * 1e-6) / 1e9
     traffic = kernel_traffic(dom, args.workload)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak_hbm, "unit": "GB/s",
                 "frac": round(achieved / peak_hbm, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
-                "launches_timed": kern[dom]["launches"]}
+                "launches_timed": kern[dom]["launches"],
+                "timing": "events at the boundaries of each run of this kernel's launches in sampled steps"}
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -364,8 +417,8 @@ def run_ours(args):
         "config": {"workload": desc, **cfg, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": ("inputs larger than L2: every step streams %.1f MB of distinct weights" % (wbytes_step / 1e6)),
                    "pdl": bool(args.pdl),
-                   "prefetch_fraction": (ops[0]["plan"].info()["prefetch_bytes"] and
-                                         (args.prefetch if args.prefetch is not None else 0.5)) if chain else 0.0},
+                   "next_weight_l2_fraction": next_frac,
+                   "side_stream_prefetch_fraction": args.prefetch if side_pf else 0.0},
         "per_projection": per_m, "roofline": roofline,
         "gpu_launches": launches_per_step * K,
     }
@@ -375,21 +428,12 @@ def run_ours(args):
     # e2e: activations from pinned host memory, outputs back, every step
     if not args.no_e2e:
         Ke = max(3, min(K, int(args.e2e_seconds / max(est, 1e-6))))
-        h2d = sum(o["hx"].numel() * 2 + (o["hres"].numel() * 2 if o["hres"] is not None else 0) for o in ops)
-        d2h = sum(o["hy"].numel() * o["hy"].element_size() for o in ops)
+        h2d, d2h = host_in.numel(), host_out.numel()
 
         def e2e_step():
-            for i, o in enumerate(ops):
-                o["x"].copy_(o["hx"], non_blocking=True)
-                if o["hres"] is not None:
-                    o["res"].copy_(o["hres"], non_blocking=True)
-                if chain and i + 1 < len(ops) and ops[i + 1]["info"]["prefetch_bytes"] > 0:
-                    side.wait_stream(stream)
-                    ops[i + 1]["plan"].prefetch(ops[i + 1]["W"], side)
-                o["plan"].run(o["x"], o["W"], o["res"], o["y"], stream)
-                if chain and i + 1 < len(ops):
-                    stream.wait_stream(side)
-                o["hy"].copy_(o["y"], non_blocking=True)
+            dev_in.copy_(host_in, non_blocking=True)
+            step()
+            host_out.copy_(dev_out, non_blocking=True)
             stream.synchronize()
         for _ in range(2):
             e2e_step()
@@ -459,7 +503,10 @@ def main(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--pdl", type=int, default=1)
     ap.add_argument("--prefetch", type=float, default=None,
-                    help="fraction of L2 filled with the next weight on a side stream (default: 0.5 for the chain, off otherwise)")
+                    help="fraction of L2 filled with the next weight by a kernel on a side stream (default: off)")
+    ap.add_argument("--next-weight", type=float, default=None,
+                    help="fraction of L2 of the next projection's weight each launch asks the L2 for "
+                         "(default: 0.15 for the chain, off otherwise)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

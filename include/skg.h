@@ -205,6 +205,19 @@ SKG_API skg_status skg_plan_set_reduction(skg_plan_t plan, int cluster);
  */
 SKG_API skg_status skg_plan_set_l2_ahead(skg_plan_t plan, int ahead);
 
+/*
+ * skg_plan_set_next_weight -- [PF] inside the launch instead of on a side
+ * stream: every later skg_run of this plan also asks the L2 (evict-last) for
+ * the first `bytes` of W_next, the weight of the projection that runs next,
+ * each CTA taking its slice once it has requested all of its own weight
+ * tiles -- so the next launch finds its first tiles cached and this launch's
+ * tail keeps HBM busy.  No extra kernel, stream or dependency is involved.
+ * bytes is rounded down to a multiple of 16 and capped at the L2 size;
+ * W_next must be 16-byte aligned and stay allocated while the plan runs.
+ * W_next == NULL or bytes == 0 turns it off.
+ */
+SKG_API skg_status skg_plan_set_next_weight(skg_plan_t plan, const void *W_next, size_t bytes);
+
 /* Fraction f in [0, 1] of the L2 that skg_prefetch_l2 fills for this plan. */
 SKG_API skg_status skg_plan_set_prefetch_fraction(skg_plan_t plan, double fraction);
 

@@ -386,6 +386,8 @@ struct skg_plan_s {
     void *ws = nullptr;               // [S*M*N] fp32 partials, then counters
     size_t ws_cap = 0;
     std::vector<void *> retired;      // outgrown workspaces: a captured graph may still use them
+    const void *next_w = nullptr;     // prefetched into L2 by this plan's launches
+    size_t next_bytes = 0;
     int gemv_ctas_per_sm = 0;         // measured occupancy of the GEMV kernel
     unsigned int *err_host = nullptr; // mapped pinned word
     unsigned int *err_dev = nullptr;
@@ -588,6 +590,17 @@ skg_status skg_plan_set_pdl(skg_plan_t p, int enable)
     return SKG_OK;
 }
 
+skg_status skg_plan_set_next_weight(skg_plan_t p, const void *W_next, size_t bytes)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_set_next_weight: plan is NULL");
+    if (W_next && !aligned(W_next, 16))
+        return fail(SKG_ERR_ALIGNMENT, "skg_plan_set_next_weight: W_next must be 16-byte aligned");
+    p->next_w = W_next;
+    p->next_bytes = W_next ? (std::min(bytes, p->l2_bytes) & ~static_cast<size_t>(15)) : 0;
+    return SKG_OK;
+}
+
 skg_status skg_plan_set_l2_ahead(skg_plan_t p, int ahead)
 {
     if (!p)
@@ -677,6 +690,8 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         g.ring = d.stages;
         g.rows_per_warp = d.split_k == 1 ? d.tile_n / (kGemvThreads / 32) : 0;
         g.ahead = d.l2_ahead;
+        g.next_w = static_cast<const unsigned char *>(p->next_w);
+        g.next_bytes = p->next_bytes;
         g.epilogue = d.epilogue;
         e = launch_gemv(g, d.grid, d.pdl != 0, s);
     } else {
@@ -705,6 +720,8 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         t.burst = d.tma_burst;
         t.cluster = d.cluster_reduce ? d.split_k : 0;
         t.ahead = d.l2_ahead;
+        t.next_w = static_cast<const unsigned char *>(p->next_w);
+        t.next_bytes = p->next_bytes;
         t.epilogue = d.epilogue;
         t.timeout_ns = kDefaultTimeoutNs;
         e = launch_splitk_tc(*mw, *mx, t, d.m_pad, d.grid, d.pdl != 0, s);

@@ -249,6 +249,8 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p)
         finish(it, g, v0, mine);
     }
     cp_async_wait<0>();                           // no copy in flight at exit
+    if (threadIdx.x == 0)
+        prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
 }
 
 // Split 1: every warp owns whole rows and runs the complete canonical tree
@@ -346,6 +348,8 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_kernel(const GemvPa
         if (lane < MM)
             store_out(p, lane, row, lane == 0 ? y.v[0] : y.v[MM - 1]);
     }
+    if (threadIdx.x == 0)
+        prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
 }
 
 // Whole rows per warp, specialised for K % 256 == 0 (every strip full):
@@ -432,6 +436,8 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_fast_kernel(const G
         if (lane < MM)
             store_out(p, lane, row, lane == 0 ? y.v[0] : y.v[MM - 1]);
     }
+    if (threadIdx.x == 0)
+        prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
 }
 
 template <int MM, int T>

@@ -49,6 +49,8 @@ struct GemvParams {
     int groups;             // ceil(N / rows_per_group)
     int ring;               // weight-ring slots per warp (2..9), split > 1
     int ahead;              // split 1: batches of the row requested into L2 ahead of use
+    const unsigned char *next_w;  // the next projection's weight, or null
+    size_t next_bytes;      // bytes of next_w the grid asks the L2 for (multiple of 16)
     int rows_per_warp;      // split 1: consecutive rows each warp computes
     int epilogue;           // skg_epilogue
 };
@@ -66,11 +68,32 @@ struct TcParams {
     int stages;             // shared-memory pipeline depth
     int burst;              // k-blocks the producer requests back to back
     int ahead;              // W tiles requested into L2 this many k-blocks ahead
+    const unsigned char *next_w;  // the next projection's weight, or null
+    size_t next_bytes;      // bytes of next_w the grid asks the L2 for (multiple of 16)
     int cluster;            // S: the S CTAs of a tile form a cluster and reduce
                             // through distributed shared memory; 0: workspace
     int epilogue;
     unsigned long long timeout_ns;
 };
+
+// The grid's share of an L2 prefetch of the next projection's weight: CTA
+// `cta` of `ctas` asks for its slice of [base, base + bytes), evict-last.
+__device__ __forceinline__ void prefetch_next_slice(const unsigned char *base, size_t bytes, unsigned cta,
+                                                    unsigned ctas, uint64_t pol)
+{
+    if (!base || bytes == 0)
+        return;
+    const size_t chunk = ((bytes + ctas - 1) / ctas + 15) & ~static_cast<size_t>(15);
+    const size_t b0 = chunk * cta;
+    if (b0 >= bytes)
+        return;
+    size_t n = bytes - b0 < chunk ? bytes - b0 : chunk;
+    for (size_t off = 0; off < n; off += 65536) {
+        const size_t k = n - off < 65536 ? n - off : 65536;
+        asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;"
+                     :: "l"(base + b0 + off), "r"(static_cast<uint32_t>(k)), "l"(pol) : "memory");
+    }
+}
 
 // Error-word bits written by kernels.
 constexpr unsigned kErrTimeoutProducer = 1u << 0;

@@ -342,6 +342,10 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 }
                 issued = i + nb;
             }
+            // Every weight tile of this CTA is requested: use the rest of the
+            // launch to ask the L2 for this CTA's slice of the next
+            // projection's weight.
+            prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
             if (flags[0]) {
                 // Abort: let every copy this thread issued land before exit.
                 for (int s = 0; s < S && s < issued; ++s) {

@@ -36,7 +36,7 @@ EXPORTS = (
     "skg_plan_query", "skg_plan", "skg_plan_force", "skg_plan_set_pdl", "skg_run",
     "skg_prefetch_l2", "skg_plan_set_prefetch_fraction", "skg_plan_info", "skg_plan_check",
     "skg_plan_destroy", "skg_debug_wait_timeout", "skg_last_error", "skg_version",
-    "skg_run_noalloc", "skg_plan_set_reduction", "skg_plan_set_l2_ahead",
+    "skg_run_noalloc", "skg_plan_set_reduction", "skg_plan_set_l2_ahead", "skg_plan_set_next_weight",
 )
 
 
@@ -92,6 +92,7 @@ def load(path: str = LIB_PATH):
     lib.skg_run_noalloc.argtypes = [i, i, i, i, vp, vp, vp, vp, vp]
     lib.skg_plan_set_reduction.argtypes = [vp, i]
     lib.skg_plan_set_l2_ahead.argtypes = [vp, i]
+    lib.skg_plan_set_next_weight.argtypes = [vp, vp, sz]
     for name in EXPORTS:
         getattr(lib, name).restype = ctypes.c_int
     lib.skg_last_error.restype = ctypes.c_char_p
@@ -155,6 +156,10 @@ def skg_plan_set_pdl(plan: int, enable: bool):
     _check(load().skg_plan_set_pdl(plan, 1 if enable else 0))
 
 
+def skg_plan_set_next_weight(plan: int, W_next, nbytes: int):
+    _check(load().skg_plan_set_next_weight(plan, _ptr(W_next), int(nbytes)))
+
+
 def skg_plan_set_l2_ahead(plan: int, ahead: int):
     _check(load().skg_plan_set_l2_ahead(plan, int(ahead)))
 
@@ -216,6 +221,9 @@ class Plan:
 
     def set_pdl(self, enable: bool):
         skg_plan_set_pdl(self.handle, enable)
+
+    def set_next_weight(self, W_next, nbytes: int):
+        skg_plan_set_next_weight(self.handle, W_next, nbytes)
 
     def set_l2_ahead(self, ahead: int):
         skg_plan_set_l2_ahead(self.handle, ahead)

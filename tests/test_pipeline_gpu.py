@@ -134,3 +134,41 @@ def test_graph_capture_of_a_chain():
     finally:
         for p in plans:
             p.close()
+
+
+@pytest.mark.parametrize("M", (1, 2, 3, 16, 64))
+def test_next_weight_prefetch_inside_the_launch(M):
+    """A plan told the next projection's weight asks the L2 for it from inside
+    its own launch: the outputs of both projections keep their bits, and the
+    setting is checked and can be turned off."""
+    cur = generate(Projection(M, 7168, 7168, "bf16", seed=80))
+    nxt = generate(Projection(M, 4096, 7168, "bf16_residual", seed=81))
+    p_cur, p_next = skg.Plan(M, 7168, 7168, "bf16"), skg.Plan(M, 4096, 7168, "bf16_residual")
+    try:
+        x, W, x2, W2, r2 = to_dev(cur.x), to_dev(cur.W), to_dev(nxt.x), to_dev(nxt.W), to_dev(nxt.res)
+        y = torch.empty(M, 7168, dtype=torch.bfloat16, device="cuda")
+        y2 = torch.empty(M, 4096, dtype=torch.bfloat16, device="cuda")
+        p_cur.run(x, W, None, y)
+        p_next.run(x2, W2, r2, y2)
+        torch.cuda.synchronize()
+        ref, ref2 = out_bits(y), out_bits(y2)
+        for nbytes in (16, 1 << 20, 2 * 4096 * 7168, 1 << 40):   # capped at the L2 size
+            p_cur.set_next_weight(W2, nbytes)
+            p_next.set_next_weight(W, nbytes)
+            for _ in range(3):
+                p_cur.run(x, W, None, y)
+                p_next.run(x2, W2, r2, y2)
+            torch.cuda.synchronize()
+            assert np.array_equal(out_bits(y), ref) and np.array_equal(out_bits(y2), ref2), nbytes
+        with pytest.raises(skg.SkgError) as e:
+            p_cur.set_next_weight(W2.data_ptr() + 2, 1 << 20)
+        assert e.value.status == skg.SKG_ERR_ALIGNMENT
+        p_cur.set_next_weight(None, 1 << 20)
+        p_cur.run(x, W, None, y)
+        torch.cuda.synchronize()
+        assert np.array_equal(out_bits(y), ref)
+        p_cur.check()
+        p_next.check()
+    finally:
+        p_cur.close()
+        p_next.close()
