@@ -82,6 +82,13 @@ void fill_gemv(skg_plan_desc *d, int split, int ring, int grid, int num_sms)
     d->workspace_bytes = 0;
     d->tma_burst = 0;
     d->threads = kGemvThreads;
+    if (split == 1 && ring >= 2) {
+        // the whole-row kernel with its weight batches moved by the copy engine
+        fill_gemv(d, 1, 0, grid, num_sms);
+        d->stages = 2;
+        d->smem_bytes = gemv_smem_bytes(d->M, d->K, 1, 2);
+        return;
+    }
     if (split == 1) {
         // whole rows per warp: tile_n = rows per CTA = 8 warps x rows per warp
         const int warps = kGemvThreads / 32;
@@ -182,7 +189,10 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
             d->from_table = 1;
         } else if (N >= 4096) {
             split = 1;   // enough rows for one warp per row
-            d->l2_ahead = 1;   // measured: the next 8-strip batch into L2 while this one loads
+            if (M == 1 && gemv_bulk_ok(M, K))
+                ring = 2;   // measured: bulk-copied batches beat 16-byte loads at M = 1
+            else
+                d->l2_ahead = 1;   // measured: the next 8-strip batch into L2 while this one loads
         } else {
             // short N: warps share rows; the smallest split whose per-warp K
             // slice fits 4-strip ring slots, then finer while N is short
@@ -538,17 +548,22 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int t
         if (d.kernel_kind == SKG_KERNEL_GEMV && split_k > 8)
             return fail(SKG_ERR_UNSUPPORTED, "the GEMV kernel supports split_k <= 8");
     }
-    if (stages != 0 && (stages < 2 || stages > (d.kernel_kind == SKG_KERNEL_GEMV ? 9 : 16)))
+    const int split = split_k ? split_k : d.split_k;
+    const bool gemv_rows = d.kernel_kind == SKG_KERNEL_GEMV && split == 1;
+    if (stages != 0 && (stages < (gemv_rows ? 1 : 2) ||
+                        stages > (gemv_rows ? 2 : (d.kernel_kind == SKG_KERNEL_GEMV ? 9 : 16))))
         return fail(SKG_ERR_INVALID_ARG, "stages=%d invalid for this plan", stages);
     if (tma_burst != 0 && (d.kernel_kind != SKG_KERNEL_SPLITK_TC || tma_burst < 1))
         return fail(SKG_ERR_INVALID_ARG, "tma_burst=%d invalid for this plan", tma_burst);
     if (grid != 0 && (d.kernel_kind != SKG_KERNEL_GEMV || grid < 1))
         return fail(SKG_ERR_INVALID_ARG, "grid=%d invalid for this plan", grid);
-    const int split = split_k ? split_k : d.split_k;
-    if (d.kernel_kind == SKG_KERNEL_GEMV && split == 1) {
-        if (stages)
-            return fail(SKG_ERR_INVALID_ARG, "split_k=1 (whole rows per warp) has no weight ring");
-        fill_gemv(&d, 1, 0, grid, p->num_sms);
+    if (gemv_rows) {
+        // stages 1: weights straight into registers; >= 2: the copy-engine
+        // ring with that many slots; 0: keep the current form
+        const int ring = stages == 1 ? 0 : (stages >= 2 ? stages : (d.split_k == 1 ? d.stages : 0));
+        if (ring >= 2 && !gemv_bulk_ok(d.M, d.K))
+            return fail(SKG_ERR_UNSUPPORTED, "the copy-engine form needs K %% 256 == 0 (M=%d K=%d)", d.M, d.K);
+        fill_gemv(&d, 1, ring, grid, p->num_sms);
     } else if (d.kernel_kind == SKG_KERNEL_GEMV) {
         int ctas = 1;
         int ring = stages ? stages : ((split_k || d.stages < 2) ? gemv_default_ring(d.M, d.K, split, &ctas) : d.stages);
@@ -689,6 +704,7 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         g.groups = (d.N + d.tile_n - 1) / d.tile_n;
         g.ring = d.stages;
         g.rows_per_warp = d.split_k == 1 ? d.tile_n / (kGemvThreads / 32) : 0;
+        g.timeout_ns = kDefaultTimeoutNs;
         g.ahead = d.l2_ahead;
         g.next_w = static_cast<const unsigned char *>(p->next_w);
         g.next_bytes = p->next_bytes;

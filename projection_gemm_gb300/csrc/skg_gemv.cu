@@ -21,6 +21,8 @@
 // chunks, so every split gives the same bits.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "skg_internal.h"
 #include "skg_ptx.cuh"
 
@@ -440,6 +442,152 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_fast_kernel(const G
         prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
 }
 
+// The whole-row kernel above with the copy engine on the load path: each
+// warp keeps one shared-memory slot of a batch (8 strips, 4 KB -- contiguous
+// in the row) and lane 0 requests the next batch with one bulk copy as soon
+// as the current batch has moved from the slot into registers, so the copy
+// overlaps the FMAs.  Compute, order and grid are those of the register
+// form, so the bits are too.  Waits are bounded; a timeout sets an error bit
+// and the warp stops after its copy in flight has landed.
+template <int MM, int JC>
+__global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const GemvParams p)
+{
+    constexpr int U = 8;                          // strips per batch
+    constexpr int B = U / JC;                     // chunks per batch
+    extern __shared__ uint4 dsm[];
+    __shared__ uint64_t wbar[kWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nch = (p.nv >> 5) / JC;             // present chunks (<= 16)
+    const int row0 = (blockIdx.x * kWarps + warp) * p.rows_per_warp;
+    const int row_end = min(p.N, row0 + p.rows_per_warp);
+    const uint64_t pol = policy_evict_first();
+    uint4 *xs = dsm;                              // [MM][nv]
+    uint4 *slot = dsm + static_cast<size_t>(MM) * p.nv + warp * U * 32;
+    uint64_t *bar = &wbar[warp];
+    uint32_t phase = 0;
+    volatile int never = 0;
+
+    // the batch starting at chunk c0 of row `row`
+    auto issue = [&](int row, int c0) {
+        if (lane == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(min(B, nch - c0) * JC) * 512u;
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_load(slot, p.W + static_cast<size_t>(row) * p.nv + c0 * JC * 32, bytes, bar, pol);
+        }
+    };
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (row0 < row_end)
+        issue(row0, 0);                           // weights are static: before the wait
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i < MM * p.nv; i += kGemvThreads)
+        xs[i] = ld_act_v4(p.x + i);
+    __syncthreads();
+
+    uint4 w[U];
+    for (int row = row0; row < row_end; ++row) {
+        const uint4 *wrow = p.W + static_cast<size_t>(row) * p.nv;
+        ChunkStack<MM> stk;
+        for (int c0 = 0; c0 < nch; c0 += B) {
+            if (p.ahead > 0 && lane == 0) {
+                const int a0 = (c0 == 0 ? B : c0 + p.ahead * B) * JC * 32;
+                const int a1 = min(nch, c0 + (p.ahead + 1) * B) * JC * 32;
+                if (a0 < a1)
+                    prefetch_l2_bulk(wrow + a0, static_cast<uint32_t>((a1 - a0) * 16), pol);
+            }
+            const bool got = mbar_wait(bar, phase, p.timeout_ns, &never);
+            phase ^= 1;
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0 && p.err)
+                    atomicOr(p.err, kErrTimeoutEpilogue);
+                mbar_wait(bar, phase ^ 1, p.timeout_ns, &never);   // let the copy land
+                return;
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                if (c0 + b < nch) {
+#pragma unroll
+                    for (int j = 0; j < JC; ++j)
+                        w[b * JC + j] = lds_v4(slot + (b * JC + j) * 32 + lane);
+                }
+            }
+            // every lane's reads of the slot come before the next copy into it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (c0 + B < nch)
+                issue(row, c0 + B);
+            else if (row + 1 < row_end)
+                issue(row + 1, 0);
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                if (c0 + b < nch) {
+                    Acc<MM> a;
+#pragma unroll
+                    for (int m = 0; m < MM; ++m)
+                        a.v[m] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < JC; ++j) {
+                        const int v = ((c0 + b) * JC + j) * 32 + lane;
+#pragma unroll
+                        for (int m = 0; m < MM; ++m)
+                            fma8(a.v[m], lds_v4(xs + m * p.nv + v), w[b * JC + j]);
+                    }
+#pragma unroll
+                    for (int m = 0; m < MM; ++m) {
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1)
+                            a.v[m] += __shfl_xor_sync(0xffffffffu, a.v[m], o);
+                    }
+                    stk.push(c0 + b, a);
+                }
+            }
+        }
+        const Acc<MM> y = stk.flush(nch);
+        if (lane < MM)
+            store_out(p, lane, row, lane == 0 ? y.v[0] : y.v[MM - 1]);
+    }
+    if (threadIdx.x == 0)
+        prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
+}
+
+template <int MM, int JC>
+cudaError_t launch_bulk_t(const GemvParams &p, const cudaLaunchConfig_t &cfg)
+{
+    static int done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kGemvMaxSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
+        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+    }
+    return cudaLaunchKernelEx(&cfg, gemv_rows_bulk_kernel<MM, JC>, p);
+}
+
+template <int MM>
+cudaError_t launch_bulk_jc(const GemvParams &p, const cudaLaunchConfig_t &cfg, int jc)
+{
+    switch (jc) {
+    case 1: return launch_bulk_t<MM, 1>(p, cfg);
+    case 2: return launch_bulk_t<MM, 2>(p, cfg);
+    case 4: return launch_bulk_t<MM, 4>(p, cfg);
+    default: return launch_bulk_t<MM, 8>(p, cfg);
+    }
+}
+
 template <int MM, int T>
 cudaError_t set_gemv_attr()
 {
@@ -552,8 +700,15 @@ int gemv_fast_jc(int K)
     return (jc == 1 || jc == 2 || jc == 4 || jc == 8) ? jc : 0;
 }
 
+bool gemv_bulk_ok(int M, int K)
+{
+    return gemv_fast_jc(K) > 0 && gemv_smem_bytes(M, K, 1, 2) <= kGemvMaxSmem;
+}
+
 int gemv_smem_bytes(int M, int K, int split, int ring)
 {
+    if (split == 1 && ring >= 2)   // copy-engine form: x + one 4 KB batch slot per warp
+        return M * K * 2 + (kGemvThreads / 32) * 8 * 512;
     if (split == 1)   // the whole-row kernels keep weights in registers; x in shared memory
         return M * K * 2;
     return M * K * 2 + (kGemvThreads / 32) * ring * gemv_tile_strips(K, split) * 512;
@@ -602,6 +757,12 @@ cudaError_t launch_gemv(const GemvParams &p, int grid, bool pdl, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    if (p.split == 1 && p.ring >= 2) {
+        const int jc = gemv_fast_jc(p.K);
+        if (!gemv_bulk_ok(p.M, p.K))
+            return cudaErrorInvalidValue;
+        return p.M == 1 ? launch_bulk_jc<1>(p, cfg, jc) : launch_bulk_jc<2>(p, cfg, jc);
+    }
     const int jc = gemv_fast_jc(p.K);
     if (p.split == 1 && jc > 0)
         return p.M == 1 ? launch_fast_jc<1>(p, cfg, jc) : launch_fast_jc<2>(p, cfg, jc);

@@ -2,9 +2,12 @@
 for profilers (ncu captures of a single kernel launch).
 
 usage: python -m projection_gemm_gb300.profile_case M N K [epilogue] [launches]
+                                                    [--split S] [--stages D]
 The operands are the seeded synthetic tensors of `inputs.py` (seed 11); the
-default plan is used; the process exits non-zero on any library error.
+default plan is used unless --split / --stages force a configuration (as
+skg_plan_force does); the process exits non-zero on any library error.
 """
+import argparse
 import sys
 
 import torch
@@ -14,9 +17,16 @@ from .inputs import Projection, generate
 
 
 def main(argv):
-    M, N, K = int(argv[0]), int(argv[1]), int(argv[2])
-    epi = argv[3] if len(argv) > 3 else "bf16"
-    launches = int(argv[4]) if len(argv) > 4 else 3
+    ap = argparse.ArgumentParser()
+    ap.add_argument("M", type=int)
+    ap.add_argument("N", type=int)
+    ap.add_argument("K", type=int)
+    ap.add_argument("epilogue", nargs="?", default="bf16")
+    ap.add_argument("launches", nargs="?", type=int, default=3)
+    ap.add_argument("--split", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
+    a = ap.parse_args(argv)
+    M, N, K, epi, launches = a.M, a.N, a.K, a.epilogue, a.launches
     build.build()
     skg.load()
     torch.cuda.set_device(0)
@@ -25,6 +35,8 @@ def main(argv):
     res = None if t.res is None else t.res.cuda()
     y = torch.empty(M, N, dtype=torch.float32 if epi == "fp32" else torch.bfloat16, device="cuda")
     plan = skg.Plan(M, N, K, epi)
+    if a.split or a.stages:
+        plan.force(split_k=a.split, stages=a.stages)
     print(plan.info())
     for _ in range(launches):
         plan.run(x, W, res, y)

@@ -44,7 +44,8 @@ def shapes():
 
 def candidates(M, N, K):
     if M <= 2:
-        c = [{"split_k": 1, "ahead": a} for a in (0, 1, 2)]
+        c = [{"split_k": 1, "stages": 1, "ahead": a} for a in (0, 1, 2)]
+        c += [{"split_k": 1, "stages": 2, "ahead": a} for a in (0, 1)]
         for split in (2, 4, 8):
             for ring in (2, 3, 4):
                 c.append({"split_k": split, "stages": ring, "ahead": 0})
@@ -125,7 +126,7 @@ def main(argv=None):
             us, cfg, info = min(results, key=lambda r: r[0])
             kind = info["kernel_kind"]
             rows.append((kind, M, N, K, skg.EPILOGUES[epi], info["split_k"],
-                         info["stages"] if kind == skg.SKG_KERNEL_SPLITK_TC or info["split_k"] > 1 else 0,
+                         info["stages"],
                          0, 1, cfg.get("ahead", 0), us, wbytes / us / 1e3))
             print(f"N={N} K={K} {epi} M={M}: best {cfg} {us:.2f} us {wbytes / us / 1e3:.0f} GB/s", flush=True)
         del Ws
@@ -133,7 +134,9 @@ def main(argv=None):
     with open(args.out_inc, "w") as f:
         f.write("// skg_plan_table.inc -- measured picker table.\n//\n"
                 "// Each row: { kernel_kind, M, N, K, epilogue, split_k, stages, grid, tma_burst, l2_ahead }.\n"
-                "// stages: TC ring stages / GEMV weight-ring slots (0 = library default);\n"
+                "// stages: TC ring stages / GEMV weight-ring slots per warp (0 = library default);\n"
+                "// GEMV split 1: 0 = 16-byte loads into registers, 2 = one bulk copy per batch into\n"
+                "// a shared-memory slot of the warp;\n"
                 "// grid = 0 lets the library size the grid.  Written by projection_gemm_gb300/tune.py\n"
                 f"// from back-to-back timings on {torch.cuda.get_device_name(0)} "
                 f"({len(rows)} rows, {time.time() - t0:.0f} s); the comment on each row is the\n"
@@ -142,7 +145,7 @@ def main(argv=None):
             f.write("{%d, %d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.2f us, %.0f GB/s\n" % r)
     if args.out_log:
         with open(args.out_log, "w") as f:
-            json.dump(log, f, indent=0)
+            f.write("[\n" + ",\n".join(json.dumps(r) for r in log) + "\n]\n")
     print(f"wrote {args.out_inc} ({len(rows)} rows)")
 
 

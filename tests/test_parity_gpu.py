@@ -91,6 +91,52 @@ def test_small_shapes_all_splits(M, N, K, epi):
         case.close()
 
 
+GEMV_FORM_SHAPES = [sh for sh in SMALL if sh[0] <= 2] + [
+    (1, 7168, 7168, "bf16"), (2, 7168, 7168, "bf16"), (2, 12288, 7168, "bf16"),
+    (1, 7168, 16384, "bf16_residual"), (2, 4096, 7168, "bf16"), (1, 384, 7168, "fp32"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,epi", GEMV_FORM_SHAPES, ids=lambda v: str(v))
+def test_gemv_row_forms_bit_identical(M, N, K, epi):
+    """Split 1 of the M <= 2 kernel has two forms -- weights loaded into
+    registers (stages 1) and, for K % 256 == 0, weights streamed by the copy
+    engine through a ring of 16 KB shared-memory slots (stages = slots, a
+    multiple of 7, the consumer warps).  Every form, ring depth and grid reproduces the bits of
+    the default plan, which meet the oracle."""
+    p = Projection(M, N, K, epi, seed=2000 + M + N + K, residual_var=1.0)
+    case = DeviceCase(p)
+    try:
+        base = case.run_bits()
+        if M * N * K <= 2 * 4096 * 4104:
+            full_check(case, base, what=f"{p} default")
+        else:
+            xb, wb, rb = case.host_bits()
+            rng = np.random.default_rng(p.seed)
+            ns, ms = rng.integers(0, N, 3000), rng.integers(0, M, 3000)
+            y_ref, s1 = O.linear_points(xb, wb, ms, ns, rb)
+            T.check(base[ms, ns], y_ref, s1, K, fp32=epi == "fp32", what=f"{p} default sampled")
+        ran = []
+        for stages, grid in ((1, 0), (2, 0), (1, 5), (2, 1), (2, 7), (2, N)):
+            try:
+                case.plan.force(split_k=1, stages=stages, grid=grid)
+            except skg.SkgError as e:
+                # the copy-engine form needs K % 256 == 0 and rings that fit
+                assert e.status == skg.SKG_ERR_UNSUPPORTED and stages >= 2, e
+                continue
+            info = case.plan.info()
+            assert info["kernel"] == "gemv" and info["split_k"] == 1
+            assert info["stages"] == (0 if stages == 1 else 2)
+            assert 1 <= info["grid"] <= N and info["threads"] == 256
+            got = case.run_bits()
+            assert np.array_equal(got, base), f"stages {stages} grid {grid} changed the bits of {p}"
+            ran.append((stages, grid))
+        assert len(ran) >= (6 if K % 256 == 0 else 2), ran
+        case.plan.check()
+    finally:
+        case.close()
+
+
 def test_pr1_config():
     p = pr1()
     case = DeviceCase(p)
