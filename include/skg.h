@@ -75,7 +75,7 @@ typedef enum skg_epilogue {
 } skg_epilogue;
 
 typedef enum skg_kernel_kind {
-    SKG_KERNEL_GEMV = 1,        /* M <= 2: CUDA-core kernel, 16-byte weight loads [TS] */
+    SKG_KERNEL_GEMV = 1,        /* M <= 2: CUDA-core kernel; weights by 16-byte loads or bulk copies [TS] */
     SKG_KERNEL_SPLITK_TC = 2    /* M > 2: TMA + tcgen05 split-K kernel [TS] */
 } skg_kernel_kind;
 
@@ -93,8 +93,11 @@ typedef struct skg_plan_desc {
     int split_k;            /* S: CTAs (TC) or warps (GEMV) sharing one output's K range; power of 2 dividing 16 */
     int tile_n;             /* W rows per output tile: 128 (TC) or rows per CTA group (GEMV) */
     int m_pad;              /* MMA N (TC: M rounded up to 16) or M (GEMV) */
-    int stages;             /* TC: shared-memory ring stages; GEMV: weight-ring slots per warp */
-    int tma_burst;          /* TC: k-blocks the TMA producer requests back to back */
+    int stages;             /* TC: shared-memory ring stages; GEMV split > 1: weight-ring slots per
+                               warp; GEMV split 1: 0 = 16-byte loads into registers, 2 = each warp's
+                               weight batches moved by bulk copies through a shared-memory slot */
+    int tma_burst;          /* TC: k-blocks the TMA producer requests back to back; GEMV split 1
+                               with bulk copies: strips (512 bytes each) per copy, 4 or 8 */
     int grid;               /* CTAs launched */
     int threads;            /* threads per CTA */
     int smem_bytes;         /* dynamic shared memory per CTA */
@@ -139,8 +142,11 @@ SKG_API skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out);
  * skg_plan_force -- override of the picker inside the plan's kernel kind
  * (used by tests and by the tuning sweep): split_k (power of 2 dividing 16;
  * TC needs 2..16, GEMV 1..8); for TC, stages (2..16, limited by shared
- * memory) and tma_burst (1..stages); for GEMV, grid (CTAs, >= 1).  A 0 keeps
- * the current value; a field that does not apply to the kind must be 0.
+ * memory) and tma_burst (1..stages); for GEMV, grid (CTAs, >= 1), and at
+ * split 1 the load path: stages 1 = 16-byte loads into registers, stages 2 =
+ * bulk copies of tma_burst (4 or 8) strips per warp batch (K % 256 == 0
+ * only; SKG_ERR_UNSUPPORTED otherwise); at split > 1, stages = ring slots
+ * (2..9).  A 0 keeps the current value; a field that does not apply must be 0.
  * If the workspace must grow, a new one is allocated and the old one is kept
  * until skg_plan_destroy, because a CUDA graph that captured skg_run of this
  * plan earlier still launches with the captured split, descriptors and

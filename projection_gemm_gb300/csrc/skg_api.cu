@@ -76,6 +76,7 @@ int gemv_default_ring(int M, int K, int split, int *ctas)
 
 void fill_gemv(skg_plan_desc *d, int split, int ring, int grid, int num_sms)
 {
+    const int want_batch = d->tma_burst;          // bulk-copy form: strips per copy asked for
     d->kernel_kind = SKG_KERNEL_GEMV;
     d->split_k = split;
     d->m_pad = d->M;
@@ -83,10 +84,13 @@ void fill_gemv(skg_plan_desc *d, int split, int ring, int grid, int num_sms)
     d->tma_burst = 0;
     d->threads = kGemvThreads;
     if (split == 1 && ring >= 2) {
-        // the whole-row kernel with its weight batches moved by the copy engine
+        // the whole-row kernel with its weight batches moved by the copy
+        // engine; tma_burst = strips per bulk copy
+        const int batch = want_batch == 4 || want_batch == 8 ? want_batch : gemv_bulk_default_batch(d->M, d->K);
         fill_gemv(d, 1, 0, grid, num_sms);
         d->stages = 2;
-        d->smem_bytes = gemv_smem_bytes(d->M, d->K, 1, 2);
+        d->tma_burst = batch;
+        d->smem_bytes = gemv_bulk_smem_bytes(d->M, d->K, batch);
         return;
     }
     if (split == 1) {
@@ -185,12 +189,13 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
             split = row->split;
             grid = row->grid;
             ring = row->stages;
+            d->tma_burst = row->burst;   // split 1 with bulk-copied batches: strips per copy
             d->l2_ahead = row->ahead;
             d->from_table = 1;
         } else if (N >= 4096) {
             split = 1;   // enough rows for one warp per row
-            if (M == 1 && gemv_bulk_ok(M, K))
-                ring = 2;   // measured: bulk-copied batches beat 16-byte loads at M = 1
+            if (gemv_bulk_ok(M, K, gemv_bulk_default_batch(M, K)))
+                ring = 2;   // measured: bulk-copied batches beat 16-byte loads at M = 1 and 2
             else
                 d->l2_ahead = 1;   // measured: the next 8-strip batch into L2 while this one loads
         } else {
@@ -553,7 +558,8 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int t
     if (stages != 0 && (stages < (gemv_rows ? 1 : 2) ||
                         stages > (gemv_rows ? 2 : (d.kernel_kind == SKG_KERNEL_GEMV ? 9 : 16))))
         return fail(SKG_ERR_INVALID_ARG, "stages=%d invalid for this plan", stages);
-    if (tma_burst != 0 && (d.kernel_kind != SKG_KERNEL_SPLITK_TC || tma_burst < 1))
+    if (tma_burst != 0 && (d.kernel_kind == SKG_KERNEL_SPLITK_TC ? tma_burst < 1
+                                                                 : !(gemv_rows && (tma_burst == 4 || tma_burst == 8))))
         return fail(SKG_ERR_INVALID_ARG, "tma_burst=%d invalid for this plan", tma_burst);
     if (grid != 0 && (d.kernel_kind != SKG_KERNEL_GEMV || grid < 1))
         return fail(SKG_ERR_INVALID_ARG, "grid=%d invalid for this plan", grid);
@@ -561,8 +567,13 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int t
         // stages 1: weights straight into registers; >= 2: the copy-engine
         // ring with that many slots; 0: keep the current form
         const int ring = stages == 1 ? 0 : (stages >= 2 ? stages : (d.split_k == 1 ? d.stages : 0));
-        if (ring >= 2 && !gemv_bulk_ok(d.M, d.K))
-            return fail(SKG_ERR_UNSUPPORTED, "the copy-engine form needs K %% 256 == 0 (M=%d K=%d)", d.M, d.K);
+        const int batch = tma_burst ? tma_burst : (d.stages >= 2 ? d.tma_burst : gemv_bulk_default_batch(d.M, d.K));
+        if (tma_burst && ring < 2)
+            return fail(SKG_ERR_INVALID_ARG, "tma_burst applies to the bulk-copy form (stages 2) only");
+        if (ring >= 2 && !gemv_bulk_ok(d.M, d.K, batch))
+            return fail(SKG_ERR_UNSUPPORTED, "the bulk-copy form needs K %% 256 == 0 and room for %d-strip batches "
+                        "(M=%d K=%d)", batch, d.M, d.K);
+        d.tma_burst = ring >= 2 ? batch : 0;
         fill_gemv(&d, 1, ring, grid, p->num_sms);
     } else if (d.kernel_kind == SKG_KERNEL_GEMV) {
         int ctas = 1;
@@ -704,6 +715,7 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         g.groups = (d.N + d.tile_n - 1) / d.tile_n;
         g.ring = d.stages;
         g.rows_per_warp = d.split_k == 1 ? d.tile_n / (kGemvThreads / 32) : 0;
+        g.batch_strips = d.tma_burst;
         g.timeout_ns = kDefaultTimeoutNs;
         g.ahead = d.l2_ahead;
         g.next_w = static_cast<const unsigned char *>(p->next_w);

@@ -443,16 +443,16 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_fast_kernel(const G
 }
 
 // The whole-row kernel above with the copy engine on the load path: each
-// warp keeps one shared-memory slot of a batch (8 strips, 4 KB -- contiguous
-// in the row) and lane 0 requests the next batch with one bulk copy as soon
+// warp keeps one shared-memory slot of a batch (U strips of 512 bytes --
+// contiguous in the row) and lane 0 requests the next batch with one bulk copy as soon
 // as the current batch has moved from the slot into registers, so the copy
 // overlaps the FMAs.  Compute, order and grid are those of the register
 // form, so the bits are too.  Waits are bounded; a timeout sets an error bit
 // and the warp stops after its copy in flight has landed.
-template <int MM, int JC>
+template <int MM, int JC, int U>
 __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const GemvParams p)
 {
-    constexpr int U = 8;                          // strips per batch
+    // U strips per batch (U * 512 bytes per copy)
     constexpr int B = U / JC;                     // chunks per batch
     extern __shared__ uint4 dsm[];
     __shared__ uint64_t wbar[kWarps];
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const G
         prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
 }
 
-template <int MM, int JC>
+template <int MM, int JC, int U>
 cudaError_t launch_bulk_t(const GemvParams &p, const cudaLaunchConfig_t &cfg)
 {
     static int done[kMaxDevices] = {};
@@ -565,26 +565,34 @@ cudaError_t launch_bulk_t(const GemvParams &p, const cudaLaunchConfig_t &cfg)
     if (dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     if (!__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) {
-        e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC, U>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kGemvMaxSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC, U>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
         __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
     }
-    return cudaLaunchKernelEx(&cfg, gemv_rows_bulk_kernel<MM, JC>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_rows_bulk_kernel<MM, JC, U>, p);
 }
 
 template <int MM>
 cudaError_t launch_bulk_jc(const GemvParams &p, const cudaLaunchConfig_t &cfg, int jc)
 {
+    if (p.batch_strips == 4) {
+        switch (jc) {
+        case 1: return launch_bulk_t<MM, 1, 4>(p, cfg);
+        case 2: return launch_bulk_t<MM, 2, 4>(p, cfg);
+        case 4: return launch_bulk_t<MM, 4, 4>(p, cfg);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (jc) {
-    case 1: return launch_bulk_t<MM, 1>(p, cfg);
-    case 2: return launch_bulk_t<MM, 2>(p, cfg);
-    case 4: return launch_bulk_t<MM, 4>(p, cfg);
-    default: return launch_bulk_t<MM, 8>(p, cfg);
+    case 1: return launch_bulk_t<MM, 1, 8>(p, cfg);
+    case 2: return launch_bulk_t<MM, 2, 8>(p, cfg);
+    case 4: return launch_bulk_t<MM, 4, 8>(p, cfg);
+    default: return launch_bulk_t<MM, 8, 8>(p, cfg);
     }
 }
 
@@ -700,15 +708,32 @@ int gemv_fast_jc(int K)
     return (jc == 1 || jc == 2 || jc == 4 || jc == 8) ? jc : 0;
 }
 
-bool gemv_bulk_ok(int M, int K)
+bool gemv_bulk_ok(int M, int K, int batch_strips)
 {
-    return gemv_fast_jc(K) > 0 && gemv_smem_bytes(M, K, 1, 2) <= kGemvMaxSmem;
+    const int jc = gemv_fast_jc(K);
+    return jc > 0 && (batch_strips == 8 || (batch_strips == 4 && jc <= 4)) &&
+           gemv_bulk_smem_bytes(M, K, batch_strips) <= kGemvMaxSmem;
+}
+
+int gemv_bulk_smem_bytes(int M, int K, int batch_strips)
+{
+    return M * K * 2 + (kGemvThreads / 32) * batch_strips * 512;   // x + one batch slot per warp
+}
+
+int gemv_bulk_default_batch(int M, int K)
+{
+    // 8-strip batches unless they cost the fourth CTA of an SM (228 KB, 1 KB
+    // reserved per CTA) and 4-strip batches would keep it
+    const int full = 4 * (gemv_bulk_smem_bytes(M, K, 8) + 1024 + 64);
+    if (full <= 233472 || !gemv_bulk_ok(M, K, 4))
+        return 8;
+    return 4;
 }
 
 int gemv_smem_bytes(int M, int K, int split, int ring)
 {
-    if (split == 1 && ring >= 2)   // copy-engine form: x + one 4 KB batch slot per warp
-        return M * K * 2 + (kGemvThreads / 32) * 8 * 512;
+    if (split == 1 && ring >= 2)   // copy-engine form at its default batch
+        return gemv_bulk_smem_bytes(M, K, gemv_bulk_default_batch(M, K));
     if (split == 1)   // the whole-row kernels keep weights in registers; x in shared memory
         return M * K * 2;
     return M * K * 2 + (kGemvThreads / 32) * ring * gemv_tile_strips(K, split) * 512;
@@ -759,8 +784,9 @@ cudaError_t launch_gemv(const GemvParams &p, int grid, bool pdl, cudaStream_t s)
     cfg.numAttrs = pdl ? 1 : 0;
     if (p.split == 1 && p.ring >= 2) {
         const int jc = gemv_fast_jc(p.K);
-        if (!gemv_bulk_ok(p.M, p.K))
+        if (!gemv_bulk_ok(p.M, p.K, p.batch_strips))
             return cudaErrorInvalidValue;
+        cfg.dynamicSmemBytes = gemv_bulk_smem_bytes(p.M, p.K, p.batch_strips);
         return p.M == 1 ? launch_bulk_jc<1>(p, cfg, jc) : launch_bulk_jc<2>(p, cfg, jc);
     }
     const int jc = gemv_fast_jc(p.K);

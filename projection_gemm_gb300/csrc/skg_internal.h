@@ -52,6 +52,7 @@ struct GemvParams {
     const unsigned char *next_w;  // the next projection's weight, or null
     size_t next_bytes;      // bytes of next_w the grid asks the L2 for (multiple of 16)
     int rows_per_warp;      // split 1: consecutive rows each warp computes
+    int batch_strips;       // split 1, bulk-copied batches: strips per copy (4 or 8)
     int epilogue;           // skg_epilogue
     unsigned long long timeout_ns;  // bounded mbarrier waits (copy-engine form)
 };
@@ -108,8 +109,10 @@ int gemv_smem_bytes(int M, int K, int split, int ring);
 int gemv_tile_strips(int K, int split);       // ring slot size in strips: 4, 8 or 16
 int gemv_fast_jc(int K);                      // >0: the specialised whole-row kernel applies
 // Split 1 with the copy engine on the load path (K % 256 == 0 and room for
-// one 4 KB batch slot per warp): selected by ring >= 2.
-bool gemv_bulk_ok(int M, int K);
+// one batch slot per warp): selected by ring >= 2; batches of 8 or 4 strips.
+bool gemv_bulk_ok(int M, int K, int batch_strips);
+int gemv_bulk_smem_bytes(int M, int K, int batch_strips);
+int gemv_bulk_default_batch(int M, int K);
 constexpr int kGemvMaxSmem = 226 * 1024;      // x (M * K * 2 bytes) + the weight rings (static smem needs the rest)
 int tc_max_stages(int m_pad, int smem_limit);
 int tc_tmem_cols(int m_pad);                  // TMEM columns one CTA allocates

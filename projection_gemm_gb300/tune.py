@@ -45,7 +45,7 @@ def shapes():
 def candidates(M, N, K):
     if M <= 2:
         c = [{"split_k": 1, "stages": 1, "ahead": a} for a in (0, 1, 2)]
-        c += [{"split_k": 1, "stages": 2, "ahead": a} for a in (0, 1)]
+        c += [{"split_k": 1, "stages": 2, "tma_burst": b, "ahead": a} for b in (4, 8) for a in (0, 1)]
         for split in (2, 4, 8):
             for ring in (2, 3, 4):
                 c.append({"split_k": split, "stages": ring, "ahead": 0})
@@ -60,7 +60,7 @@ def time_config(M, N, K, epi, cfg, Ws, x, res, y, rounds):
     p = None
     try:
         p = skg.Plan(M, N, K, epi)
-        force = {k: v for k, v in cfg.items() if k in ("split_k", "stages") and v}
+        force = {k: v for k, v in cfg.items() if k in ("split_k", "stages", "tma_burst") and v}
         p.force(**force)
         p.set_l2_ahead(cfg.get("ahead", 0))
         for W in Ws[:2]:
@@ -127,7 +127,9 @@ def main(argv=None):
             kind = info["kernel_kind"]
             rows.append((kind, M, N, K, skg.EPILOGUES[epi], info["split_k"],
                          info["stages"],
-                         0, 1, cfg.get("ahead", 0), us, wbytes / us / 1e3))
+                         0, info["tma_burst"] if kind == skg.SKG_KERNEL_SPLITK_TC or
+                         (info["split_k"] == 1 and info["stages"] >= 2) else 1,
+                         cfg.get("ahead", 0), us, wbytes / us / 1e3))
             print(f"N={N} K={K} {epi} M={M}: best {cfg} {us:.2f} us {wbytes / us / 1e3:.0f} GB/s", flush=True)
         del Ws
         torch.cuda.empty_cache()
@@ -136,7 +138,7 @@ def main(argv=None):
                 "// Each row: { kernel_kind, M, N, K, epilogue, split_k, stages, grid, tma_burst, l2_ahead }.\n"
                 "// stages: TC ring stages / GEMV weight-ring slots per warp (0 = library default);\n"
                 "// GEMV split 1: 0 = 16-byte loads into registers, 2 = one bulk copy per batch into\n"
-                "// a shared-memory slot of the warp;\n"
+                "// a shared-memory slot of the warp (tma_burst = strips per copy there);\n"
                 "// grid = 0 lets the library size the grid.  Written by projection_gemm_gb300/tune.py\n"
                 f"// from back-to-back timings on {torch.cuda.get_device_name(0)} "
                 f"({len(rows)} rows, {time.time() - t0:.0f} s); the comment on each row is the\n"
