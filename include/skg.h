@@ -130,8 +130,8 @@ SKG_API skg_status skg_plan_query(int M, int N, int K, int epilogue, int num_sms
  * skg_plan -- build a plan for (M,N,K,epilogue) on the current CUDA device.
  * Picks the kernel as skg_plan_query does and allocates a mapped host word for
  * device-side error reports; a tensor-core plan that reduces through its
- * global workspace (see skg_plan_set_reduction) also allocates S*M*N fp32
- * partials plus one zeroed counter per 128-row tile.  The plan must be
+ * global workspace (see skg_plan_set_reduction) also allocates S x ceil(N/128)
+ * x M x 128 fp32 partials plus one zeroed counter per 128-row tile.  The plan must be
  * freed with skg_plan_destroy.  One skg_run of a plan may be in flight at a
  * time (the workspace is shared); concurrent streams need separate plans.
  * Errors: as skg_plan_query, plus SKG_ERR_CUDA.  *out is NULL on failure.

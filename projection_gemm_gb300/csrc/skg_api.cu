@@ -133,7 +133,7 @@ void fill_tc(skg_plan_desc *d, int split, int stages, int burst)
     const int n_tiles = (d->N + kTileN - 1) / kTileN;
     d->grid = n_tiles * split;
     d->workspace_bytes = d->cluster_reduce ? 0
-                                           : static_cast<size_t>(split) * d->M * d->N * sizeof(float) +
+                                           : tc_partial_bytes(d->M, d->N, split) +
                                                  static_cast<size_t>(n_tiles) * sizeof(unsigned int);
 }
 
@@ -359,11 +359,11 @@ skg_status prepare_splitk_launch(int M, int N, int K, int epi, const void *x, co
         return fail(SKG_ERR_UNSUPPORTED, "N=%d needs %d arrival counters; the static scratch has %d", N, n_tiles,
                     max_tiles);
     int split = d.split_k;
-    while (split > 2 && static_cast<size_t>(split) * M * N * sizeof(float) > scratch_bytes)
+    while (split > 2 && tc_partial_bytes(M, N, split) > scratch_bytes)
         split /= 2;
-    if (static_cast<size_t>(split) * M * N * sizeof(float) > scratch_bytes)
+    if (tc_partial_bytes(M, N, split) > scratch_bytes)
         return fail(SKG_ERR_UNSUPPORTED, "M*N=%lld needs %zu bytes of partials at split 2; the static scratch holds %zu",
-                    static_cast<long long>(M) * N, static_cast<size_t>(2) * M * N * sizeof(float), scratch_bytes);
+                    static_cast<long long>(M) * N, tc_partial_bytes(M, N, 2), scratch_bytes);
     if (split != d.split_k)
         fill_tc(&d, split, d.stages, d.tma_burst);
     st = encode_2d(tmW, W, N, K, kTileN);
@@ -398,7 +398,7 @@ struct skg_plan_s {
     int num_sms = 0;
     size_t l2_bytes = 0;
     double prefetch_fraction = 0.5;
-    void *ws = nullptr;               // [S*M*N] fp32 partials, then counters
+    void *ws = nullptr;               // [S][tiles][M][128] fp32 partials, then counters
     size_t ws_cap = 0;
     std::vector<void *> retired;      // outgrown workspaces: a captured graph may still use them
     const void *next_w = nullptr;     // prefetched into L2 by this plan's launches
@@ -736,7 +736,7 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         t.y = y;
         t.ws = static_cast<float *>(p->ws);
         t.counters = reinterpret_cast<unsigned int *>(static_cast<char *>(p->ws) +
-                                                      static_cast<size_t>(d.split_k) * d.M * d.N * sizeof(float));
+                                                      tc_partial_bytes(d.M, d.N, d.split_k));
         t.err = p->err_dev;
         t.M = d.M;
         t.N = d.N;

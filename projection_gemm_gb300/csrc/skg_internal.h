@@ -103,6 +103,12 @@ constexpr unsigned kErrTimeoutMma = 1u << 1;
 constexpr unsigned kErrTimeoutEpilogue = 1u << 2;
 constexpr unsigned kErrTimeoutDebug = 1u << 3;
 
+// Bytes of fp32 split-K partials: S x ceil(N / 128) tiles x [M][128].
+inline size_t tc_partial_bytes(int M, int N, int split)
+{
+    return static_cast<size_t>(split) * ((N + kTileN - 1) / kTileN) * kTileN * M * sizeof(float);
+}
+
 // Shared-memory bytes of the tensor-core kernel for (m_pad, stages).
 int tc_smem_bytes(int m_pad, int stages);
 int gemv_smem_bytes(int M, int K, int split, int ring);

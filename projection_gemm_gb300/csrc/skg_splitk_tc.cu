@@ -149,6 +149,12 @@ __device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)
     tmem_wait_st();
 }
 
+// The workspace holds, for every split s and tile, the tile's partial sums
+// as one contiguous block [M][128] of fp32 (m-major, the tile's 128 rows
+// innermost): a warp's stores and loads of one column m are coalesced, and a
+// tile's S partials are S compact blocks instead of M x S row pieces spread
+// N floats apart (measured: 29.3 -> 25.0 us at M = 64, K = N = 7168).
+//
 // The last CTA of a tile: y[m, n] for this thread's row n and columns
 // [half * NC, half * NC + NC) from the S split values in the workspace,
 // combined by the top levels of the canonical tree.  Loads are issued in
@@ -156,8 +162,10 @@ __device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)
 // the register budget of the CTA shape allows), so the tile costs a few L2
 // round trips instead of one per column.
 template <int S, int NC>
-__device__ __forceinline__ void reduce_tile(const TcParams &p, int n, int half, int sp)
+__device__ __forceinline__ void reduce_tile(const TcParams &p, int tile, int row, int half, int sp)
 {
+    const int n = tile * kTileN + row;
+
     constexpr int kLoads = NC >= 24 ? 48 : 24;
     constexpr int G0 = kLoads / S < 1 ? 1 : kLoads / S;
     constexpr int G = G0 < NC ? G0 : NC;                 // columns per batch
@@ -173,7 +181,7 @@ __device__ __forceinline__ void reduce_tile(const TcParams &p, int n, int half, 
             for (int s = 0; s < S; ++s) {
                 const int m = mb + g;
                 v[g][s] = (s < sp && m < p.M)
-                              ? __ldcg(&p.ws[(static_cast<size_t>(s) * p.M + m) * p.N + n])
+                              ? __ldcg(&p.ws[((static_cast<size_t>(s) * p.n_tiles + tile) * p.M + m) * kTileN + row])
                               : 0.f;
             }
         }
@@ -491,7 +499,7 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 for (int c = 0; c < NC; ++c) {
                     const int m = half * NC + c;
                     if (m < p.M)
-                        p.ws[(static_cast<size_t>(split) * p.M + m) * p.N + n] = cur[c];
+                        p.ws[((static_cast<size_t>(split) * p.n_tiles + tile) * p.M + m) * kTileN + row] = cur[c];
                 }
             }
             // Arrive on the tile's counter: the barrier orders every epilogue
@@ -508,10 +516,10 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 const int sp = (total_present + L - 1) / L;  // splits holding a value
                 if (n < p.N) {
                     switch (p.split) {
-                    case 2: reduce_tile<2, NC>(p, n, half, sp); break;
-                    case 4: reduce_tile<4, NC>(p, n, half, sp); break;
-                    case 8: reduce_tile<8, NC>(p, n, half, sp); break;
-                    default: reduce_tile<16, NC>(p, n, half, sp); break;
+                    case 2: reduce_tile<2, NC>(p, tile, row, half, sp); break;
+                    case 4: reduce_tile<4, NC>(p, tile, row, half, sp); break;
+                    case 8: reduce_tile<8, NC>(p, tile, row, half, sp); break;
+                    default: reduce_tile<16, NC>(p, tile, row, half, sp); break;
                     }
                 }
                 if (ew == 0 && lane == 0)
