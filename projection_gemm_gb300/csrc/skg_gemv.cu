@@ -482,6 +482,7 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const G
     __syncwarp();
     if (row0 < row_end)
         issue(row0, 0);                           // weights are static: before the wait
+    __syncwarp();                                 // lane 0 issued alone: reconverge before the CTA barrier
     pdl_wait();
     pdl_launch_dependents();
     for (int i = threadIdx.x; i < MM * p.nv; i += kGemvThreads)

@@ -547,6 +547,10 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         cluster_sync();   // no CTA leaves while a peer still reads its memory
     }
 
+    // Lane 0 of the producer and MMA warps ran their roles alone: reconverge
+    // each warp before the CTA barrier, so every warp arrives whole and TMEM
+    // is freed only after every role is done.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
