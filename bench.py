@@ -316,18 +316,19 @@ def run_ours(args):
             g0 = i
     group_start = {a: j for j, (a, _) in enumerate(groups)}
 
-    def step(events=None, mode="launch"):
+    def step(events=None, mode="launch", s=None):
+        s = stream if s is None else s
         for i, o in enumerate(ops):
             if side_pf and i + 1 < len(ops) and ops[i + 1]["info"]["prefetch_bytes"] > 0:
-                side.wait_stream(stream)
+                side.wait_stream(s)
                 ops[i + 1]["plan"].prefetch(ops[i + 1]["W"], side)
             if events is not None and (mode == "launch" or i in group_start):
-                events[i if mode == "launch" else group_start[i]].record(stream)
-            o["plan"].run(o["x"], o["W"], o["res"], o["y"], stream)
+                events[i if mode == "launch" else group_start[i]].record(s)
+            o["plan"].run(o["x"], o["W"], o["res"], o["y"], s)
             if side_pf and i + 1 < len(ops):
-                stream.wait_stream(side)
+                s.wait_stream(side)
         if events is not None:
-            events[-1].record(stream)
+            events[-1].record(s)
 
     launches_per_step = len(ops) + (sum(1 for o in ops[1:] if o["info"]["prefetch_bytes"] > 0) if side_pf else 0)
     wbytes_step = sum(o["p"].weight_bytes() for o in ops)
@@ -339,6 +340,24 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
     est = (time.perf_counter() - t0) / warm
+    # --graph: a step's launches captured once into a CUDA graph (skg_run
+    # allocates nothing; the programmatic launch edges are kept) and replayed
+    # each step, so the host issues one launch per step.  Steps that carry
+    # events run eagerly.
+    graph = None
+    if args.graph and not side_pf:
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            step(s=cap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            step(s=cap)
+        torch.cuda.synchronize()
+        for _ in range(warm):
+            graph.replay()
+        torch.cuda.synchronize()
     K = args.steps if args.steps else max(20, min(40000, int(args.seconds / max(est, 1e-6))))
     # Sampled steps carry events, alternately before every launch (the
     # us/projection figures) or at kernel-kind boundaries only (each kind's
@@ -364,7 +383,10 @@ def run_ours(args):
     w0 = time.time()
     start.record(stream)
     for k in range(K):
-        step(evs.get(k), modes.get(k, "launch"))
+        if graph is not None and k not in evs:
+            graph.replay()
+        else:
+            step(evs.get(k), modes.get(k, "launch"))
     end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
@@ -417,6 +439,8 @@ def run_ours(args):
         "config": {"workload": desc, **cfg, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": ("inputs larger than L2: every step streams %.1f MB of distinct weights" % (wbytes_step / 1e6)),
                    "pdl": bool(args.pdl),
+                   "launch": ("cuda graph of the step's launches, replayed (steps carrying events run eagerly)"
+                              if graph is not None else "eager skg_run calls"),
                    "next_weight_l2_fraction": next_frac,
                    "side_stream_prefetch_fraction": args.prefetch if side_pf else 0.0},
         "per_projection": per_m, "roofline": roofline,
@@ -502,6 +526,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--pdl", type=int, default=1)
+    ap.add_argument("--graph", type=int, default=0,
+                    help="1: replay each step as one captured CUDA graph (measured slower: replays do not overlap)")
     ap.add_argument("--prefetch", type=float, default=None,
                     help="fraction of L2 filled with the next weight by a kernel on a side stream (default: off)")
     ap.add_argument("--next-weight", type=float, default=None,

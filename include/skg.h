@@ -105,8 +105,9 @@ typedef struct skg_plan_desc {
     size_t workspace_bytes; /* split-K partials + counters owned by the plan */
     size_t prefetch_bytes;  /* bytes skg_prefetch_l2 touches for this plan's W */
     int pdl;                /* 1: launched with programmatic dependent launch */
-    int l2_ahead;           /* weights requested into L2 ahead of use: TC k-blocks beyond the
-                               ring, GEMV (split 1) batches of 8 strips; 0 = none */
+    int l2_ahead;           /* weights requested into L2 ahead of use: TC k-blocks after the
+                               ring, before the wait for the previous kernel; GEMV (split 1)
+                               batches of the row; 0 = none */
     int cluster_reduce;     /* TC: 1 = the split_k CTAs of a tile form a thread-block cluster and
                                reduce through distributed shared memory (no workspace);
                                0 = fp32 partials in the plan's workspace, last CTA reduces */
@@ -203,10 +204,13 @@ SKG_API skg_status skg_prefetch_l2(skg_plan_t next, const void *W_next, void *si
 SKG_API skg_status skg_plan_set_reduction(skg_plan_t plan, int cluster);
 
 /*
- * skg_plan_set_l2_ahead -- [PF] applied inside a kernel: each weight tile
- * (TC: 128 x 64 k-block; GEMV split 1: 8-strip batch of a row) is also
- * requested into L2 `ahead` tiles before it is loaded, without using shared
- * memory or registers.  0..16; 0 turns it off.  The GEMV ring kernel
+ * skg_plan_set_l2_ahead -- [PF] applied inside a kernel, without shared
+ * memory or registers.  TC: before waiting for the previous kernel in the
+ * stream, each CTA also requests the `ahead` weight tiles (128 x 64
+ * k-blocks) that follow its ring into L2, so the previous kernel's tail
+ * keeps HBM busy with this launch's weights.  GEMV split 1: each batch of a
+ * row is also requested into L2 `ahead` batches before it is loaded (the
+ * first ones before the wait).  0..16; 0 turns it off.  The GEMV ring kernel
  * (split > 1) ignores it.
  */
 SKG_API skg_status skg_plan_set_l2_ahead(skg_plan_t plan, int ahead);

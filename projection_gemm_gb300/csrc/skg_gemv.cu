@@ -480,8 +480,17 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const G
         fence_mbar_init();
     }
     __syncwarp();
-    if (row0 < row_end)
+    if (row0 < row_end) {
         issue(row0, 0);                           // weights are static: before the wait
+        if (p.ahead > 0 && lane == 0) {
+            // and the next `ahead` batches of the row into L2, while the
+            // previous kernel finishes
+            const int a0 = B * JC * 32, a1 = min(nch, (p.ahead + 1) * B) * JC * 32;
+            if (a0 < a1)
+                prefetch_l2_bulk(p.W + static_cast<size_t>(row0) * p.nv + a0, static_cast<uint32_t>((a1 - a0) * 16),
+                                 pol);
+        }
+    }
     __syncwarp();                                 // lane 0 issued alone: reconverge before the CTA barrier
     pdl_wait();
     pdl_launch_dependents();
@@ -494,7 +503,7 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const G
         const uint4 *wrow = p.W + static_cast<size_t>(row) * p.nv;
         ChunkStack<MM> stk;
         for (int c0 = 0; c0 < nch; c0 += B) {
-            if (p.ahead > 0 && lane == 0) {
+            if (p.ahead > 0 && lane == 0 && !(row == row0 && c0 == 0)) {   // row0's first request: above
                 const int a0 = (c0 == 0 ? B : c0 + p.ahead * B) * JC * 32;
                 const int a1 = min(nch, c0 + (p.ahead + 1) * B) * JC * 32;
                 if (a0 < a1)

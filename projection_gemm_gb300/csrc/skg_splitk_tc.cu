@@ -308,15 +308,16 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
             const int pre = nk < S ? nk : S;
-            // W tiles beyond the ring are requested into L2 `ahead` k-blocks
-            // in advance (weights only: allowed before the wait below)
-            for (int i = pre; i < nk && i < pre + p.ahead; ++i)
-                tma_prefetch_l2_2d(&tmW, (kb_begin + i) * kBlockK, tile * kTileN);
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full[i], kWBytes + Sh::kXBytes);
                 tma_load_2d(sW + i * kWBytes, &tmW, &full[i], (kb_begin + i) * kBlockK,
                             tile * kTileN, pol_w);
             }
+            // While the previous kernel finishes, the `ahead` W tiles after the
+            // ring are requested into L2 too (weights only: allowed before the
+            // wait below), so its tail keeps HBM busy with this launch's bytes.
+            for (int i = pre; i < nk && i < pre + p.ahead; ++i)
+                tma_prefetch_l2_2d(&tmW, (kb_begin + i) * kBlockK, tile * kTileN);
             pdl_wait();  // activations only from here on
             for (int i = 0; i < pre; ++i)
                 tma_load_2d(sX + i * Sh::kXBytes, &tmX, &full[i], (kb_begin + i) * kBlockK, 0, pol_x);
@@ -341,8 +342,6 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                     break;
                 for (int j = 0; j < nb; ++j) {
                     const int s = (i + j) % S;
-                    if (p.ahead > 0 && i + j + p.ahead < nk)
-                        tma_prefetch_l2_2d(&tmW, (kb_begin + i + j + p.ahead) * kBlockK, tile * kTileN);
                     mbar_arrive_expect_tx(&full[s], kWBytes + Sh::kXBytes);
                     tma_load_2d(sW + s * kWBytes, &tmW, &full[s], (kb_begin + i + j) * kBlockK,
                                 tile * kTileN, pol_w);

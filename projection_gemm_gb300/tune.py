@@ -45,12 +45,13 @@ def shapes():
 def candidates(M, N, K):
     if M <= 2:
         c = [{"split_k": 1, "stages": 1, "ahead": a} for a in (0, 1, 2)]
-        c += [{"split_k": 1, "stages": 2, "tma_burst": b, "ahead": a} for b in (4, 8) for a in (0, 1)]
+        c += [{"split_k": 1, "stages": 2, "tma_burst": b, "ahead": a} for b in (4, 8) for a in (0, 1, 2)]
         for split in (2, 4, 8):
             for ring in (2, 3, 4):
                 c.append({"split_k": split, "stages": ring, "ahead": 0})
         return c
-    return [{"split_k": s, "stages": st, "ahead": 0} for s in (2, 4, 8, 16) for st in (3, 4, 5, 6)]
+    return [{"split_k": s, "stages": st, "ahead": a} for s in (2, 4, 8, 16) for st in (3, 4, 5, 6)
+            for a in (0, 2, 4, 6, 8)]
 
 
 def time_config(M, N, K, epi, cfg, Ws, x, res, y, rounds):
