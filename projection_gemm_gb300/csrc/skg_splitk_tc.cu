@@ -201,6 +201,86 @@ __device__ __forceinline__ void reduce_tile(const TcParams &p, int tile, int row
     }
 }
 
+// The last CTA of a tile, with 16-byte loads: work item (m, g) is rows
+// 4g..4g+3 of column m, so the 32 lanes of a warp read 512 contiguous bytes
+// of each split's block, and each output is combined exactly as in
+// reduce_tile (the top levels of the canonical tree, in index order).  The
+// 256 epilogue threads take items et, et + 256, ...; IB = L / S items per
+// batch keep L loads in flight (L as the CTA shape's register budget allows).
+__device__ __forceinline__ void store_out4(const TcParams &p, int m, int n0, int cnt, const float4 &v)
+{
+    const size_t idx = static_cast<size_t>(m) * p.N + n0;
+    const float a[4] = {v.x, v.y, v.z, v.w};
+    if (cnt == 4 && (p.N & 3) == 0) {
+        if (p.epilogue == SKG_EPI_FP32) {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.y) + idx) = v;
+            return;
+        }
+        float b[4] = {a[0], a[1], a[2], a[3]};
+        if (p.epilogue == SKG_EPI_BF16_RESIDUAL) {
+            const uint2 r = *reinterpret_cast<const uint2 *>(p.res + idx);
+            b[0] += bf16lo(r.x);
+            b[1] += bf16hi(r.x);
+            b[2] += bf16lo(r.y);
+            b[3] += bf16hi(r.y);
+        }
+        uint2 o;
+        o.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b[0]))) |
+              (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b[1]))) << 16);
+        o.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b[2]))) |
+              (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b[3]))) << 16);
+        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.y) + idx) = o;
+        return;
+    }
+    for (int i = 0; i < cnt; ++i)
+        store_out(p, m, n0 + i, a[i]);
+}
+
+template <int S, int L>
+__device__ __forceinline__ void reduce_tile_v4(const TcParams &p, int tile, int sp, int et)
+{
+    constexpr int IB = S >= L ? 1 : L / S;        // items per batch
+    const int rows = min(kTileN, p.N - tile * kTileN);
+    const int items = p.M * (kTileN / 4);
+    const float *base = p.ws + static_cast<size_t>(tile) * p.M * kTileN;
+    const size_t sstride = static_cast<size_t>(p.n_tiles) * p.M * kTileN;
+#pragma unroll 1
+    for (int i0 = et; i0 < items; i0 += kEpiThreads * IB) {
+        float4 v[IB][S];
+#pragma unroll
+        for (int b = 0; b < IB; ++b) {
+            const int it = i0 + b * kEpiThreads;
+            const int m = it >> 5, g = it & 31;
+#pragma unroll
+            for (int s = 0; s < S; ++s) {
+                v[b][s] = (s < sp && it < items && 4 * g < rows)
+                              ? __ldcg(reinterpret_cast<const float4 *>(base + s * sstride + m * kTileN + 4 * g))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < IB; ++b) {
+            const int it = i0 + b * kEpiThreads;
+            const int m = it >> 5, g = it & 31;
+            if (it >= items || 4 * g >= rows)
+                continue;
+#pragma unroll
+            for (int stride = 1; stride < S; stride <<= 1) {
+#pragma unroll
+                for (int i = 0; i + stride < S; i += 2 * stride) {
+                    if (i + stride < sp) {
+                        v[b][i].x = v[b][i].x + v[b][i + stride].x;
+                        v[b][i].y = v[b][i].y + v[b][i + stride].y;
+                        v[b][i].z = v[b][i].z + v[b][i + stride].z;
+                        v[b][i].w = v[b][i].w + v[b][i + stride].w;
+                    }
+                }
+            }
+            store_out4(p, m, tile * kTileN + 4 * g, min(4, rows - 4 * g), v[b][0]);
+        }
+    }
+}
+
 // Cluster mode: CTA `rank` of the tile's cluster produces rows
 // [rank * 128/S, (rank+1) * 128/S) of the tile for every column m, reading
 // the S subtree values from the S CTAs' shared memory in index order and
@@ -513,13 +593,16 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             epi_bar_sync();
             if (flags[1]) {
                 const int sp = (total_present + L - 1) / L;  // splits holding a value
-                if (n < p.N) {
-                    switch (p.split) {
-                    case 2: reduce_tile<2, NC>(p, tile, row, half, sp); break;
-                    case 4: reduce_tile<4, NC>(p, tile, row, half, sp); break;
-                    case 8: reduce_tile<8, NC>(p, tile, row, half, sp); break;
-                    default: reduce_tile<16, NC>(p, tile, row, half, sp); break;
-                    }
+                const int et = threadIdx.x - 64;
+                constexpr int kL = MPAD <= 32 ? 8 : 16;   // 16-byte loads in flight per thread
+                switch (p.split) {
+                case 2: reduce_tile_v4<2, kL>(p, tile, sp, et); break;
+                case 4: reduce_tile_v4<4, kL>(p, tile, sp, et); break;
+                case 8: reduce_tile_v4<8, kL>(p, tile, sp, et); break;
+                default:
+                    if (n < p.N)
+                        reduce_tile<16, NC>(p, tile, row, half, sp);
+                    break;
                 }
                 if (ew == 0 && lane == 0)
                     p.counters[tile] = 0;
