@@ -95,7 +95,9 @@ typedef struct skg_plan_desc {
     int m_pad;              /* MMA N (TC: M rounded up to 16) or M (GEMV) */
     int stages;             /* TC: shared-memory ring stages; GEMV split > 1: weight-ring slots per
                                warp; GEMV split 1: 0 = 16-byte loads into registers, 2 = each warp's
-                               weight batches moved by bulk copies through a shared-memory slot */
+                               weight batches moved by bulk copies through a shared-memory slot,
+                               whole rows per warp; 3 = the same in one balanced wave (CTAs own row
+                               runs, warps equal runs of chunks, rows combined in shared memory) */
     int tma_burst;          /* TC: k-blocks the TMA producer requests back to back; GEMV split 1
                                with bulk copies: strips (512 bytes each) per copy, 4 or 8 */
     int grid;               /* CTAs launched */
@@ -145,9 +147,10 @@ SKG_API skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out);
  * TC needs 2..16, GEMV 1..8); for TC, stages (2..16, limited by shared
  * memory) and tma_burst (1..stages); for GEMV, grid (CTAs, >= 1), and at
  * split 1 the load path: stages 1 = 16-byte loads into registers, stages 2 =
- * bulk copies of tma_burst (4 or 8) strips per warp batch (K % 256 == 0
- * only; SKG_ERR_UNSUPPORTED otherwise); at split > 1, stages = ring slots
- * (2..9).  A 0 keeps the current value; a field that does not apply must be 0.
+ * bulk copies of tma_burst (4 or 8) strips per warp batch, stages 3 = the
+ * same batches in one balanced wave (grid <= N, at most 256 rows per CTA)
+ * (K % 256 == 0 only; SKG_ERR_UNSUPPORTED otherwise); at split > 1, stages =
+ * ring slots (2..9).  A 0 keeps the current value; a field that does not apply must be 0.
  * If the workspace must grow, a new one is allocated and the old one is kept
  * until skg_plan_destroy, because a CUDA graph that captured skg_run of this
  * plan earlier still launches with the captured split, descriptors and

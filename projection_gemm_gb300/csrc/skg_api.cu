@@ -83,6 +83,18 @@ void fill_gemv(skg_plan_desc *d, int split, int ring, int grid, int num_sms)
     d->workspace_bytes = 0;
     d->tma_burst = 0;
     d->threads = kGemvThreads;
+    if (split == 1 && ring == 3) {
+        // one balanced wave: CTAs own row runs, warps equal runs of chunks
+        const int batch = want_batch == 4 || want_batch == 8 ? want_batch : gemv_bulk_default_batch(d->M, d->K);
+        d->split_k = 1;
+        d->stages = 3;
+        d->tma_burst = batch;
+        d->threads = kGemvThreads;
+        d->grid = grid > 0 ? std::min(grid, d->N) : gemv_span_grid(d->M, d->N, d->K, batch, num_sms);
+        d->tile_n = (d->N + d->grid - 1) / d->grid;
+        d->smem_bytes = gemv_span_smem_bytes(d->M, d->K, batch, d->tile_n);
+        return;
+    }
     if (split == 1 && ring >= 2) {
         // the whole-row kernel with its weight batches moved by the copy
         // engine; tma_burst = strips per bulk copy
@@ -194,8 +206,10 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
             d->from_table = 1;
         } else if (N >= 4096) {
             split = 1;   // enough rows for one warp per row
+            // measured: bulk-copied batches beat 16-byte loads at M = 1 and 2;
+            // at M = 1 one balanced wave beats whole rows per warp
             if (gemv_bulk_ok(M, K, gemv_bulk_default_batch(M, K)))
-                ring = 2;   // measured: bulk-copied batches beat 16-byte loads at M = 1 and 2
+                ring = M == 1 ? 3 : 2;
             else
                 d->l2_ahead = 1;   // measured: the next 8-strip batch into L2 while this one loads
         } else {
@@ -557,7 +571,7 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int t
     const int split = split_k ? split_k : d.split_k;
     const bool gemv_rows = d.kernel_kind == SKG_KERNEL_GEMV && split == 1;
     if (stages != 0 && (stages < (gemv_rows ? 1 : 2) ||
-                        stages > (gemv_rows ? 2 : (d.kernel_kind == SKG_KERNEL_GEMV ? 9 : 16))))
+                        stages > (gemv_rows ? 3 : (d.kernel_kind == SKG_KERNEL_GEMV ? 9 : 16))))
         return fail(SKG_ERR_INVALID_ARG, "stages=%d invalid for this plan", stages);
     if (tma_burst != 0 && (d.kernel_kind == SKG_KERNEL_SPLITK_TC ? tma_burst < 1
                                                                  : !(gemv_rows && (tma_burst == 4 || tma_burst == 8))))
@@ -574,8 +588,13 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int t
         if (ring >= 2 && !gemv_bulk_ok(d.M, d.K, batch))
             return fail(SKG_ERR_UNSUPPORTED, "the bulk-copy form needs K %% 256 == 0 and room for %d-strip batches "
                         "(M=%d K=%d)", batch, d.M, d.K);
+        if (ring == 3 && grid && (d.N + std::min(grid, d.N) - 1) / std::min(grid, d.N) > kGemvSpanMaxRows)
+            return fail(SKG_ERR_UNSUPPORTED, "the one-wave form takes at most %d rows per CTA (N=%d, grid=%d)",
+                        kGemvSpanMaxRows, d.N, grid);
         d.tma_burst = ring >= 2 ? batch : 0;
         fill_gemv(&d, 1, ring, grid, p->num_sms);
+        if (ring == 3 && d.smem_bytes > kGemvMaxSmem)
+            return fail(SKG_ERR_UNSUPPORTED, "the one-wave form does not fit shared memory at M=%d K=%d", d.M, d.K);
     } else if (d.kernel_kind == SKG_KERNEL_GEMV) {
         int ctas = 1;
         int ring = stages ? stages : ((split_k || d.stages < 2) ? gemv_default_ring(d.M, d.K, split, &ctas) : d.stages);

@@ -564,6 +564,190 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const G
         prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
 }
 
+// Split 1 in one balanced wave: the grid is as many CTAs as the SMs hold,
+// CTA b owns rows [b N / grid, (b+1) N / grid) and each of its warps an
+// equal contiguous run of the CTA's canonical chunks -- rows are adjacent in
+// memory, so a run crosses row boundaries freely and is still streamed in
+// bulk-copied batches of U strips (as in the kernel above).  Every chunk sum
+// is computed exactly as in the other forms and stored in shared memory;
+// after one CTA barrier each row's sums are combined by the same balanced
+// tree (absent chunks skipped), so the bits are the same.  No row is split
+// across CTAs, so there is no cross-CTA step.
+template <int MM, int JC, int U>
+__global__ void __launch_bounds__(kGemvThreads, 4) gemv_span_kernel(const GemvParams p)
+{
+    constexpr int B = U / JC;                     // chunks per batch
+    extern __shared__ uint4 dsm[];
+    __shared__ uint64_t wbar[kWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nch = (p.nv >> 5) / JC;             // chunks per row (<= 16)
+    const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.N / gridDim.x);
+    const int r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.N / gridDim.x);
+    const int total = (r1 - r0) * nch;
+    const int g0 = static_cast<int>(static_cast<long long>(warp) * total / kWarps);
+    const int g1 = static_cast<int>(static_cast<long long>(warp + 1) * total / kWarps);
+    const uint64_t pol = policy_evict_first();
+    uint4 *xs = dsm;                              // [MM][nv]
+    uint4 *slot = dsm + static_cast<size_t>(MM) * p.nv + warp * U * 32;
+    float *sums = reinterpret_cast<float *>(dsm + static_cast<size_t>(MM) * p.nv + kWarps * U * 32);  // [rows][16][MM]
+    const uint4 *wbase = p.W + static_cast<size_t>(r0) * p.nv;   // chunk g starts at vector g * JC * 32
+    uint64_t *bar = &wbar[warp];
+    uint32_t phase = 0;
+    volatile int never = 0;
+
+    auto issue = [&](int g) {
+        if (lane == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(min(B, g1 - g) * JC) * 512u;
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_load(slot, wbase + static_cast<size_t>(g) * JC * 32, bytes, bar, pol);
+        }
+    };
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (g0 < g1) {
+        issue(g0);                                // weights are static: before the wait
+        if (p.ahead > 0 && lane == 0) {
+            const int a0 = g0 + B, a1 = min(g1, g0 + (p.ahead + 1) * B);
+            if (a0 < a1)
+                prefetch_l2_bulk(wbase + static_cast<size_t>(a0) * JC * 32, static_cast<uint32_t>((a1 - a0) * JC) * 512u,
+                                 pol);
+        }
+    }
+    __syncwarp();
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i < MM * p.nv; i += kGemvThreads)
+        xs[i] = ld_act_v4(p.x + i);
+    __syncthreads();
+
+    uint4 w[U];
+    bool ok = true;
+    for (int gb = g0; gb < g1; gb += B) {
+        if (p.ahead > 0 && lane == 0 && gb > g0) {
+            const int a0 = gb + p.ahead * B, a1 = min(g1, gb + (p.ahead + 1) * B);
+            if (a0 < a1)
+                prefetch_l2_bulk(wbase + static_cast<size_t>(a0) * JC * 32, static_cast<uint32_t>((a1 - a0) * JC) * 512u,
+                                 pol);
+        }
+        const bool got = mbar_wait(bar, phase, p.timeout_ns, &never);
+        phase ^= 1;
+        if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0 && p.err)
+                atomicOr(p.err, kErrTimeoutEpilogue);
+            mbar_wait(bar, phase ^ 1, p.timeout_ns, &never);   // let the copy land
+            ok = false;
+            break;
+        }
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            if (gb + b < g1) {
+#pragma unroll
+                for (int j = 0; j < JC; ++j)
+                    w[b * JC + j] = lds_v4(slot + (b * JC + j) * 32 + lane);
+            }
+        }
+        // every lane's reads of the slot come before the next copy into it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (gb + B < g1)
+            issue(gb + B);
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const int g = gb + b;
+            if (g < g1) {
+                const int row = g / nch, c = g - row * nch;
+                Acc<MM> a;
+#pragma unroll
+                for (int m = 0; m < MM; ++m)
+                    a.v[m] = 0.f;
+#pragma unroll
+                for (int j = 0; j < JC; ++j) {
+                    const int v = (c * JC + j) * 32 + lane;
+#pragma unroll
+                    for (int m = 0; m < MM; ++m)
+                        fma8(a.v[m], lds_v4(xs + m * p.nv + v), w[b * JC + j]);
+                }
+#pragma unroll
+                for (int m = 0; m < MM; ++m) {
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1)
+                        a.v[m] += __shfl_xor_sync(0xffffffffu, a.v[m], o);
+                }
+                if (lane < MM)
+                    sums[(row * kChunks + c) * MM + lane] = lane == 0 ? a.v[0] : a.v[MM - 1];
+            }
+        }
+    }
+    __syncwarp();
+    ok = __syncthreads_and(ok);
+    if (ok) {
+        // each row's chunk sums by the balanced tree over 16 leaves, absent ones skipped
+        for (int t = threadIdx.x; t < (r1 - r0) * MM; t += kGemvThreads) {
+            const int row = t / MM, m = t - row * MM;
+            float v[kChunks];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+                v[c] = c < nch ? sums[(row * kChunks + c) * MM + m] : 0.f;
+#pragma unroll
+            for (int stride = 1; stride < kChunks; stride <<= 1) {
+#pragma unroll
+                for (int i = 0; i + stride < kChunks; i += 2 * stride) {
+                    if (i + stride < nch)
+                        v[i] = v[i] + v[i + stride];
+                }
+            }
+            store_out(p, m, r0 + row, v[0]);
+        }
+    }
+    if (threadIdx.x == 0)
+        prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
+}
+
+template <int MM, int JC, int U>
+cudaError_t launch_span_t(const GemvParams &p, const cudaLaunchConfig_t &cfg)
+{
+    static int done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(gemv_span_kernel<MM, JC, U>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kGemvMaxSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_span_kernel<MM, JC, U>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
+        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+    }
+    return cudaLaunchKernelEx(&cfg, gemv_span_kernel<MM, JC, U>, p);
+}
+
+template <int MM>
+cudaError_t launch_span_jc(const GemvParams &p, const cudaLaunchConfig_t &cfg, int jc)
+{
+    if (p.batch_strips == 4) {
+        switch (jc) {
+        case 1: return launch_span_t<MM, 1, 4>(p, cfg);
+        case 2: return launch_span_t<MM, 2, 4>(p, cfg);
+        case 4: return launch_span_t<MM, 4, 4>(p, cfg);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (jc) {
+    case 1: return launch_span_t<MM, 1, 8>(p, cfg);
+    case 2: return launch_span_t<MM, 2, 8>(p, cfg);
+    case 4: return launch_span_t<MM, 4, 8>(p, cfg);
+    default: return launch_span_t<MM, 8, 8>(p, cfg);
+    }
+}
+
 template <int MM, int JC, int U>
 cudaError_t launch_bulk_t(const GemvParams &p, const cudaLaunchConfig_t &cfg)
 {
@@ -730,6 +914,28 @@ int gemv_bulk_smem_bytes(int M, int K, int batch_strips)
     return M * K * 2 + (kGemvThreads / 32) * batch_strips * 512;   // x + one batch slot per warp
 }
 
+int gemv_span_smem_bytes(int M, int K, int batch_strips, int rows_per_cta)
+{
+    // x + one batch slot per warp + the chunk sums of the CTA's rows
+    return gemv_bulk_smem_bytes(M, K, batch_strips) + rows_per_cta * kChunks * M * 4;
+}
+
+int gemv_span_grid(int M, int N, int K, int batch_strips, int num_sms)
+{
+    // one wave: as many CTAs as the SMs hold (228 KB, 1 KB reserved per CTA,
+    // at most 4 by the launch bounds), never fewer than N / kGemvSpanMaxRows
+    int grid = 0;
+    for (int ctas = 4; ctas >= 1 && grid == 0; --ctas) {
+        const int g = std::min(N, ctas * num_sms);
+        const int rows = (N + g - 1) / g;
+        if (rows <= kGemvSpanMaxRows && ctas * (gemv_span_smem_bytes(M, K, batch_strips, rows) + 1024 + 64) <= 233472)
+            grid = g;
+    }
+    if (grid == 0)
+        grid = std::min(N, std::max(num_sms, (N + kGemvSpanMaxRows - 1) / kGemvSpanMaxRows));
+    return grid;
+}
+
 int gemv_bulk_default_batch(int M, int K)
 {
     // 8-strip batches unless they cost the fourth CTA of an SM (228 KB, 1 KB
@@ -742,8 +948,8 @@ int gemv_bulk_default_batch(int M, int K)
 
 int gemv_smem_bytes(int M, int K, int split, int ring)
 {
-    if (split == 1 && ring >= 2)   // copy-engine form at its default batch
-        return gemv_bulk_smem_bytes(M, K, gemv_bulk_default_batch(M, K));
+    if (split == 1 && ring >= 2)   // copy-engine forms at the default batch (span: one row per CTA)
+        return gemv_bulk_smem_bytes(M, K, gemv_bulk_default_batch(M, K)) + (ring == 3 ? kChunks * M * 4 : 0);
     if (split == 1)   // the whole-row kernels keep weights in registers; x in shared memory
         return M * K * 2;
     return M * K * 2 + (kGemvThreads / 32) * ring * gemv_tile_strips(K, split) * 512;
@@ -792,6 +998,16 @@ cudaError_t launch_gemv(const GemvParams &p, int grid, bool pdl, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    if (p.split == 1 && p.ring == 3) {
+        const int jc = gemv_fast_jc(p.K);
+        const int rows = (p.N + grid - 1) / grid;
+        if (!gemv_bulk_ok(p.M, p.K, p.batch_strips) || grid > p.N || rows > kGemvSpanMaxRows)
+            return cudaErrorInvalidValue;
+        cfg.dynamicSmemBytes = gemv_span_smem_bytes(p.M, p.K, p.batch_strips, rows);
+        if (cfg.dynamicSmemBytes > static_cast<size_t>(kGemvMaxSmem))
+            return cudaErrorInvalidValue;
+        return p.M == 1 ? launch_span_jc<1>(p, cfg, jc) : launch_span_jc<2>(p, cfg, jc);
+    }
     if (p.split == 1 && p.ring >= 2) {
         const int jc = gemv_fast_jc(p.K);
         if (!gemv_bulk_ok(p.M, p.K, p.batch_strips))

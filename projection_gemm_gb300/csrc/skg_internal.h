@@ -119,6 +119,10 @@ int gemv_fast_jc(int K);                      // >0: the specialised whole-row k
 bool gemv_bulk_ok(int M, int K, int batch_strips);
 int gemv_bulk_smem_bytes(int M, int K, int batch_strips);
 int gemv_bulk_default_batch(int M, int K);
+// Split 1 in one balanced wave (ring == 3): CTAs own row runs, warps equal chunk runs.
+constexpr int kGemvSpanMaxRows = 256;
+int gemv_span_smem_bytes(int M, int K, int batch_strips, int rows_per_cta);
+int gemv_span_grid(int M, int N, int K, int batch_strips, int num_sms);
 constexpr int kGemvMaxSmem = 226 * 1024;      // x (M * K * 2 bytes) + the weight rings (static smem needs the rest)
 int tc_max_stages(int m_pad, int smem_limit);
 int tc_tmem_cols(int m_pad);                  // TMEM columns one CTA allocates

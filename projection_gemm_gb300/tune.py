@@ -45,7 +45,8 @@ def shapes():
 def candidates(M, N, K):
     if M <= 2:
         c = [{"split_k": 1, "stages": 1, "ahead": a} for a in (0, 1, 2)]
-        c += [{"split_k": 1, "stages": 2, "tma_burst": b, "ahead": a} for b in (4, 8) for a in (0, 1, 2)]
+        c += [{"split_k": 1, "stages": st, "tma_burst": b, "ahead": a} for st in (2, 3) for b in (4, 8)
+              for a in (0, 1, 2)]
         for split in (2, 4, 8):
             for ring in (2, 3, 4):
                 c.append({"split_k": split, "stages": ring, "ahead": 0})
@@ -139,7 +140,8 @@ def main(argv=None):
                 "// Each row: { kernel_kind, M, N, K, epilogue, split_k, stages, grid, tma_burst, l2_ahead }.\n"
                 "// stages: TC ring stages / GEMV weight-ring slots per warp (0 = library default);\n"
                 "// GEMV split 1: 0 = 16-byte loads into registers, 2 = one bulk copy per batch into\n"
-                "// a shared-memory slot of the warp (tma_burst = strips per copy there);\n"
+                "// a shared-memory slot of the warp, whole rows per warp, 3 = the same batches in one\n"
+                "// balanced wave (tma_burst = strips per copy for 2 and 3);\n"
                 "// grid = 0 lets the library size the grid.  Written by projection_gemm_gb300/tune.py\n"
                 f"// from back-to-back timings on {torch.cuda.get_device_name(0)} "
                 f"({len(rows)} rows, {time.time() - t0:.0f} s); the comment on each row is the\n"
