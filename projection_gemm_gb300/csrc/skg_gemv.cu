@@ -4,10 +4,22 @@
 // details 1 "Tune shapes for the workload": at batch 1-2 the attention input
 // projections run on specialised small-matrix kernels.  At M <= 2 a
 // projection is a pure weight stream (one or two FMAs per weight loaded), so
-// this kernel is built for HBM bandwidth: every weight byte is read once with
-// 16-byte coalesced loads (L1 no-allocate, L2 evict-first), several loads per
-// lane are in flight before any is used, and accumulation is fp32 on CUDA
-// cores -- tensor cores would idle at this arithmetic intensity.
+// this kernel is built for HBM bandwidth: every weight byte is read once
+// (L2 evict-first), many bytes per SM are in flight before any is used, and
+// accumulation is fp32 on CUDA cores -- tensor cores would idle at this
+// arithmetic intensity.
+//
+// Forms, all with the arithmetic order below (so the same bits):
+//   gemv_kernel            split 2..8: warps share a row's K range, per-lane
+//                          cp.async ring, cross-warp combine (short N)
+//   gemv_rows_kernel       split 1, any K: whole rows per warp, 16-byte loads
+//                          into registers
+//   gemv_rows_fast_kernel  the same for K % 256 == 0 (chunk width fixed)
+//   gemv_rows_bulk_kernel  the same with each warp's weight batches moved by
+//                          bulk copies into a shared-memory slot (default M = 2)
+//   gemv_span_kernel       the bulk-copied batches in one balanced wave: CTAs
+//                          own row runs, warps equal chunk runs, rows combined
+//                          in shared memory (default M = 1)
 //
 // Reduction order (fixed, independent of the launch shape): row n is read in
 // strips of 32 16-byte vectors (one coalesced 512-byte warp load; lane l
