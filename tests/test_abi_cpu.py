@@ -91,3 +91,32 @@ def test_null_arguments_are_rejected():
     assert lib.skg_plan_destroy(None) == skg.SKG_OK
     assert lib.skg_plan_query(4, 128, 128, 0, SMS, L2, None) == skg.SKG_ERR_INVALID_ARG
     assert lib.skg_prefetch_l2(None, None, None) == skg.SKG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("N,K", [(5120, 5120), (8192, 2048), (4608, 3072)])
+def test_default_rule_for_shapes_outside_the_table(N, K):
+    """Shapes the measured table does not list fall back to the documented
+    rules: at M = 1 the one-wave bulk-copy GEMV, at M = 2 whole rows per warp
+    with bulk-copied batches (both need K % 256 == 0), and for M > 2 the
+    split-K kernel with its W tiles after the ring requested into L2 before
+    the wait for the previous kernel."""
+    d1 = skg.skg_plan_query(1, N, K, "bf16", SMS, L2)
+    assert d1["from_table"] == 0 and d1["kernel"] == "gemv" and d1["split_k"] == 1
+    assert d1["stages"] == 3 and d1["threads"] == 256
+    assert 1 <= d1["grid"] <= 4 * SMS and d1["tile_n"] == -(-N // d1["grid"])
+    d2 = skg.skg_plan_query(2, N, K, "bf16", SMS, L2)
+    assert d2["from_table"] == 0 and d2["stages"] == 2 and d2["tma_burst"] in (4, 8)
+    assert d2["grid"] == -(-N // 8)
+    d8 = skg.skg_plan_query(8, N, K, "bf16", SMS, L2)
+    assert d8["from_table"] == 0 and d8["kernel"] == "splitk_tc" and d8["l2_ahead"] == 2
+
+
+def test_register_loads_when_k_is_not_a_multiple_of_256():
+    d = skg.skg_plan_query(1, 5120, 5128, "bf16", SMS, L2)
+    assert d["kernel"] == "gemv" and d["split_k"] == 1 and d["stages"] == 0
+
+
+def test_one_wave_grid_keeps_rows_per_cta_bounded():
+    # a very tall weight: at most 256 rows per CTA, so the grid grows past one wave
+    d = skg.skg_plan_query(1, 300000, 1024, "bf16", SMS, L2)
+    assert d["stages"] == 3 and -(-300000 // d["grid"]) <= 256
