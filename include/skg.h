@@ -211,10 +211,11 @@ SKG_API skg_status skg_plan_set_reduction(skg_plan_t plan, int cluster);
  * memory or registers.  TC: before waiting for the previous kernel in the
  * stream, each CTA also requests the `ahead` weight tiles (128 x 64
  * k-blocks) that follow its ring into L2, so the previous kernel's tail
- * keeps HBM busy with this launch's weights.  GEMV split 1: each batch of a
- * row is also requested into L2 `ahead` batches before it is loaded (the
- * first ones before the wait).  0..16; 0 turns it off.  The GEMV ring kernel
- * (split > 1) ignores it.
+ * keeps HBM busy with this launch's weights.  GEMV split 1 with 16-byte
+ * loads (stages 0) or in one wave (stages 3): each batch is also requested
+ * into L2 `ahead` batches before it is loaded (the first ones before the
+ * wait).  0..16; 0 turns it off.  The GEMV ring kernel (split > 1) and the
+ * whole-row bulk-copy form (stages 2) ignore it.
  */
 SKG_API skg_status skg_plan_set_l2_ahead(skg_plan_t plan, int ahead);
 

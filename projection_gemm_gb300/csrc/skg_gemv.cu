@@ -454,17 +454,56 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_fast_kernel(const G
         prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
 }
 
-// The whole-row kernel above with the copy engine on the load path: each
-// warp keeps one shared-memory slot of a batch (U strips of 512 bytes --
-// contiguous in the row) and lane 0 requests the next batch with one bulk copy as soon
-// as the current batch has moved from the slot into registers, so the copy
-// overlaps the FMAs.  Compute, order and grid are those of the register
-// form, so the bits are too.  Waits are bounded; a timeout sets an error bit
-// and the warp stops after its copy in flight has landed.
+// Lane reduction of a whole row at once.  Each lane holds V = 16 * MM
+// partial sums (index m * 16 + c: chunk c, batch row m).  At each xor step
+// 16, 8, 4, 2, 1 a lane keeps one half of its values and adds its partner's
+// copy of that half, so every value is summed over the same lane pairs, in
+// the same order, as by an xor butterfly of its own: the bits equal 16 * MM
+// separate butterflies at a tenth of the shuffles.  Afterwards lane l holds
+// value l >> (5 - log2 V); then the chunk sums of each m are combined across
+// lanes by the balanced tree over 16 leaves (absent chunks skipped).  Returns
+// the row sum for m = lane >> 4 (MM = 2, lanes 0 and 16) or m = 0 (MM = 1,
+// lane 0).
+template <int MM>
+__device__ __forceinline__ float reduce_row(float (&v)[kChunks * MM], int lane, int nch)
+{
+    constexpr int V = kChunks * MM;
+    constexpr int LS = 32 / V;                    // lanes per value at the end (1 or 2)
+#pragma unroll
+    for (int n = V, o = 16; n > 1; n >>= 1, o >>= 1) {
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = hi ? v[i + n / 2] : v[i];
+            const float send = hi ? v[i] : v[i + n / 2];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float r = v[0];
+    if (LS == 2)
+        r += __shfl_xor_sync(0xffffffffu, r, 1);  // the last butterfly step, both lanes of a value
+    const int c = (lane / LS) & (kChunks - 1);
+#pragma unroll
+    for (int st = 1; st < kChunks; st <<= 1) {
+        const float partner = __shfl_xor_sync(0xffffffffu, r, st * LS);
+        if ((c & (2 * st - 1)) == 0 && c + st < nch)
+            r = r + partner;
+    }
+    return r;
+}
+
+// Whole rows per warp with the copy engine on the load path: each warp keeps
+// one shared-memory slot of a batch (U strips of 512 bytes, contiguous in the
+// row) and lane 0 requests the next batch with one bulk copy as soon as the
+// current batch has moved from the slot into registers, so the copy overlaps
+// the FMAs.  The row's 16 x MM chunk sums stay per lane (fresh fp32
+// accumulators, vectors in strip order as in the other forms) and are reduced
+// once per row by reduce_row rather than one butterfly and tree step per
+// chunk: the same bits, about a tenth of the shuffles.  Waits are bounded; a
+// timeout sets an error bit and the warp stops after its copy has landed.
 template <int MM, int JC, int U>
 __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const GemvParams p)
 {
-    // U strips per batch (U * 512 bytes per copy)
     constexpr int B = U / JC;                     // chunks per batch
     extern __shared__ uint4 dsm[];
     __shared__ uint64_t wbar[kWarps];
@@ -479,7 +518,6 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const G
     uint32_t phase = 0;
     volatile int never = 0;
 
-    // the batch starting at chunk c0 of row `row`
     auto issue = [&](int row, int c0) {
         if (lane == 0) {
             const uint32_t bytes = static_cast<uint32_t>(min(B, nch - c0) * JC) * 512u;
@@ -492,88 +530,106 @@ __global__ void __launch_bounds__(kGemvThreads, 4) gemv_rows_bulk_kernel(const G
         fence_mbar_init();
     }
     __syncwarp();
-    if (row0 < row_end) {
+    if (row0 < row_end)
         issue(row0, 0);                           // weights are static: before the wait
-        if (p.ahead > 0 && lane == 0) {
-            // and the next `ahead` batches of the row into L2, while the
-            // previous kernel finishes
-            const int a0 = B * JC * 32, a1 = min(nch, (p.ahead + 1) * B) * JC * 32;
-            if (a0 < a1)
-                prefetch_l2_bulk(p.W + static_cast<size_t>(row0) * p.nv + a0, static_cast<uint32_t>((a1 - a0) * 16),
-                                 pol);
-        }
-    }
-    __syncwarp();                                 // lane 0 issued alone: reconverge before the CTA barrier
+    __syncwarp();
     pdl_wait();
     pdl_launch_dependents();
     for (int i = threadIdx.x; i < MM * p.nv; i += kGemvThreads)
         xs[i] = ld_act_v4(p.x + i);
     __syncthreads();
 
-    uint4 w[U];
     for (int row = row0; row < row_end; ++row) {
-        const uint4 *wrow = p.W + static_cast<size_t>(row) * p.nv;
-        ChunkStack<MM> stk;
-        for (int c0 = 0; c0 < nch; c0 += B) {
-            if (p.ahead > 0 && lane == 0 && !(row == row0 && c0 == 0)) {   // row0's first request: above
-                const int a0 = (c0 == 0 ? B : c0 + p.ahead * B) * JC * 32;
-                const int a1 = min(nch, c0 + (p.ahead + 1) * B) * JC * 32;
-                if (a0 < a1)
-                    prefetch_l2_bulk(wrow + a0, static_cast<uint32_t>((a1 - a0) * 16), pol);
-            }
-            const bool got = mbar_wait(bar, phase, p.timeout_ns, &never);
-            phase ^= 1;
-            if (!__all_sync(0xffffffffu, got)) {
-                if (lane == 0 && p.err)
-                    atomicOr(p.err, kErrTimeoutEpilogue);
-                mbar_wait(bar, phase ^ 1, p.timeout_ns, &never);   // let the copy land
-                return;
-            }
+        float acc[kChunks * MM];
 #pragma unroll
-            for (int b = 0; b < B; ++b) {
-                if (c0 + b < nch) {
+        for (int i = 0; i < kChunks * MM; ++i)
+            acc[i] = 0.f;
+        uint4 w[U];
 #pragma unroll
-                    for (int j = 0; j < JC; ++j)
-                        w[b * JC + j] = lds_v4(slot + (b * JC + j) * 32 + lane);
+        for (int c = 0; c < kChunks; ++c) {
+            if (c < nch) {
+                if (c % B == 0) {
+                    const bool got = mbar_wait(bar, phase, p.timeout_ns, &never);
+                    phase ^= 1;
+                    if (!__all_sync(0xffffffffu, got)) {
+                        if (lane == 0 && p.err)
+                            atomicOr(p.err, kErrTimeoutEpilogue);
+                        mbar_wait(bar, phase ^ 1, p.timeout_ns, &never);   // let the copy land
+                        return;
+                    }
+#pragma unroll
+                    for (int b = 0; b < B; ++b) {
+                        if (c + b < nch) {
+#pragma unroll
+                            for (int j = 0; j < JC; ++j)
+                                w[b * JC + j] = lds_v4(slot + (b * JC + j) * 32 + lane);
+                        }
+                    }
+                    // every lane's reads of the slot come before the next copy into it
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (c + B < nch)
+                        issue(row, c + B);
+                    else if (row + 1 < row_end)
+                        issue(row + 1, 0);
                 }
-            }
-            // every lane's reads of the slot come before the next copy into it
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (c0 + B < nch)
-                issue(row, c0 + B);
-            else if (row + 1 < row_end)
-                issue(row + 1, 0);
 #pragma unroll
-            for (int b = 0; b < B; ++b) {
-                if (c0 + b < nch) {
-                    Acc<MM> a;
+                for (int j = 0; j < JC; ++j) {
+                    const int v = (c * JC + j) * 32 + lane;
 #pragma unroll
                     for (int m = 0; m < MM; ++m)
-                        a.v[m] = 0.f;
-#pragma unroll
-                    for (int j = 0; j < JC; ++j) {
-                        const int v = ((c0 + b) * JC + j) * 32 + lane;
-#pragma unroll
-                        for (int m = 0; m < MM; ++m)
-                            fma8(a.v[m], lds_v4(xs + m * p.nv + v), w[b * JC + j]);
-                    }
-#pragma unroll
-                    for (int m = 0; m < MM; ++m) {
-#pragma unroll
-                        for (int o = 16; o >= 1; o >>= 1)
-                            a.v[m] += __shfl_xor_sync(0xffffffffu, a.v[m], o);
-                    }
-                    stk.push(c0 + b, a);
+                        fma8(acc[m * kChunks + c], lds_v4(xs + m * p.nv + v), w[(c % B) * JC + j]);
                 }
             }
         }
-        const Acc<MM> y = stk.flush(nch);
-        if (lane < MM)
-            store_out(p, lane, row, lane == 0 ? y.v[0] : y.v[MM - 1]);
+        const float r = reduce_row<MM>(acc, lane, nch);
+        if ((lane & 15) == 0 && (lane >> 4) < MM)
+            store_out(p, lane >> 4, row, r);
     }
     if (threadIdx.x == 0)
         prefetch_next_slice(p.next_w, p.next_bytes, blockIdx.x, gridDim.x, policy_evict_last());
+}
+
+template <int MM, int JC, int U>
+cudaError_t launch_bulk_t(const GemvParams &p, const cudaLaunchConfig_t &cfg)
+{
+    static int done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC, U>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kGemvMaxSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC, U>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
+        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+    }
+    return cudaLaunchKernelEx(&cfg, gemv_rows_bulk_kernel<MM, JC, U>, p);
+}
+
+template <int MM>
+cudaError_t launch_bulk_jc(const GemvParams &p, const cudaLaunchConfig_t &cfg, int jc)
+{
+    if (p.batch_strips == 4) {
+        switch (jc) {
+        case 1: return launch_bulk_t<MM, 1, 4>(p, cfg);
+        case 2: return launch_bulk_t<MM, 2, 4>(p, cfg);
+        case 4: return launch_bulk_t<MM, 4, 4>(p, cfg);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (jc) {
+    case 1: return launch_bulk_t<MM, 1, 8>(p, cfg);
+    case 2: return launch_bulk_t<MM, 2, 8>(p, cfg);
+    case 4: return launch_bulk_t<MM, 4, 8>(p, cfg);
+    default: return launch_bulk_t<MM, 8, 8>(p, cfg);
+    }
 }
 
 // Split 1 in one balanced wave: the grid is as many CTAs as the SMs hold,
@@ -760,47 +816,6 @@ cudaError_t launch_span_jc(const GemvParams &p, const cudaLaunchConfig_t &cfg, i
     }
 }
 
-template <int MM, int JC, int U>
-cudaError_t launch_bulk_t(const GemvParams &p, const cudaLaunchConfig_t &cfg)
-{
-    static int done[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    if (!__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) {
-        e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC, U>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kGemvMaxSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_rows_bulk_kernel<MM, JC, U>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess)
-            return e;
-        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
-    }
-    return cudaLaunchKernelEx(&cfg, gemv_rows_bulk_kernel<MM, JC, U>, p);
-}
-
-template <int MM>
-cudaError_t launch_bulk_jc(const GemvParams &p, const cudaLaunchConfig_t &cfg, int jc)
-{
-    if (p.batch_strips == 4) {
-        switch (jc) {
-        case 1: return launch_bulk_t<MM, 1, 4>(p, cfg);
-        case 2: return launch_bulk_t<MM, 2, 4>(p, cfg);
-        case 4: return launch_bulk_t<MM, 4, 4>(p, cfg);
-        default: return cudaErrorInvalidValue;
-        }
-    }
-    switch (jc) {
-    case 1: return launch_bulk_t<MM, 1, 8>(p, cfg);
-    case 2: return launch_bulk_t<MM, 2, 8>(p, cfg);
-    case 4: return launch_bulk_t<MM, 4, 8>(p, cfg);
-    default: return launch_bulk_t<MM, 8, 8>(p, cfg);
-    }
-}
 
 template <int MM, int T>
 cudaError_t set_gemv_attr()

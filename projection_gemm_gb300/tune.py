@@ -45,8 +45,8 @@ def shapes():
 def candidates(M, N, K):
     if M <= 2:
         c = [{"split_k": 1, "stages": 1, "ahead": a} for a in (0, 1, 2)]
-        c += [{"split_k": 1, "stages": st, "tma_burst": b, "ahead": a} for st in (2, 3) for b in (4, 8)
-              for a in (0, 1, 2)]
+        c += [{"split_k": 1, "stages": 2, "tma_burst": b, "ahead": 0} for b in (4, 8)]
+        c += [{"split_k": 1, "stages": 3, "tma_burst": b, "ahead": a} for b in (4, 8) for a in (0, 1, 2)]
         for split in (2, 4, 8):
             for ring in (2, 3, 4):
                 c.append({"split_k": split, "stages": ring, "ahead": 0})
