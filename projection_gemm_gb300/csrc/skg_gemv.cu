@@ -1035,7 +1035,7 @@ cudaError_t launch_gemv(const GemvParams &p, int grid, bool pdl, cudaStream_t s)
             return cudaErrorInvalidValue;
         return p.M == 1 ? launch_span_jc<1>(p, cfg, jc) : launch_span_jc<2>(p, cfg, jc);
     }
-    if (p.split == 1 && p.ring >= 2) {
+    if (p.split == 1 && p.ring == 2) {
         const int jc = gemv_fast_jc(p.K);
         if (!gemv_bulk_ok(p.M, p.K, p.batch_strips))
             return cudaErrorInvalidValue;

@@ -47,14 +47,15 @@ struct GemvParams {
     int split;              // warps per output row (1, 2, 4, 8)
     int rows_per_group;     // 8 / split
     int groups;             // ceil(N / rows_per_group)
-    int ring;               // weight-ring slots per warp (2..9), split > 1
+    int ring;               // split > 1: weight-ring slots per warp (2..9); split 1: the form --
+                            // 0 16-byte loads, 2 whole rows with bulk-copied batches, 3 one wave
     int ahead;              // split 1: batches of the row requested into L2 ahead of use
     const unsigned char *next_w;  // the next projection's weight, or null
     size_t next_bytes;      // bytes of next_w the grid asks the L2 for (multiple of 16)
     int rows_per_warp;      // split 1: consecutive rows each warp computes
     int batch_strips;       // split 1, bulk-copied batches: strips per copy (4 or 8)
     int epilogue;           // skg_epilogue
-    unsigned long long timeout_ns;  // bounded mbarrier waits (copy-engine form)
+    unsigned long long timeout_ns;  // bounded mbarrier waits (bulk-copy forms)
 };
 
 struct TcParams {
