@@ -341,11 +341,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     est = (time.perf_counter() - t0) / warm
     # --graph: a step's launches captured once into a CUDA graph (skg_run
-    # allocates nothing; the programmatic launch edges are kept) and replayed
-    # each step, so the host issues one launch per step.  Steps that carry
-    # events run eagerly.
+    # allocates nothing; the programmatic launch edges are kept, and a
+    # side-stream prefetch becomes a forked node joined before the next
+    # projection) and replayed each step, so the host issues one launch per
+    # step.  Steps that carry events run eagerly.
     graph = None
-    if args.graph and not side_pf:
+    if args.graph:
         cap = torch.cuda.Stream(device=dev)
         cap.wait_stream(stream)
         with torch.cuda.stream(cap):
@@ -353,7 +354,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap):
-            step(s=cap)
+            step(s=cap)   # the side stream forks from and joins back into the capture
+        side.wait_stream(stream)
         torch.cuda.synchronize()
         for _ in range(warm):
             graph.replay()
