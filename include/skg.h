@@ -291,6 +291,54 @@ SKG_API const char *skg_last_error(void);
 /* SKG_VERSION of the loaded library. */
 SKG_API int skg_version(void);
 
+/*
+ * Groups -- several projections of the same M (3..64) in one persistent
+ * split-K launch.  [OC] fuses producer and consumer in one kernel across
+ * GPUs; this is the one-GPU form of that idea: the launch's CTAs take the
+ * work units (projection, 128-row tile, split) in projection order, keep
+ * their TMA ring, TMEM and barriers from one unit to the next, and stream
+ * the next projection's weights while the previous one is still being
+ * reduced, so consecutive projections pay no launch head or tail between
+ * them.  Each projection's output has the bits of skg_run at the same split
+ * (splits above 8 are lowered to 8: any split gives the same bits).
+ *
+ * skg_group -- plan n (1..8) projections: N[i], K[i] and epilogue[i] as for
+ * skg_plan; dep[i] (i >= 1; dep may be NULL for none) = 1: projection i
+ * reads its x and residual only after projection i - 1 has written all of
+ * its y (an on-device counter, bounded wait) -- set it whenever projection
+ * i consumes projection i - 1's output.  Projections without dep read their
+ * inputs with no ordering against the rest of the group, so their x,
+ * residual and y must not be written by another projection of the group.
+ * Projection 0 reads x only after the previous kernel in the stream
+ * (programmatic dependent launch, as skg_run).  Allocates the partials and
+ * counters of every projection.  Errors: SKG_ERR_INVALID_ARG,
+ * SKG_ERR_UNSUPPORTED (n, M or a shape outside the limits), SKG_ERR_CUDA.
+ */
+typedef struct skg_group_s *skg_group_t;
+SKG_API skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilogue, const int *dep,
+                             skg_group_t *out);
+
+/*
+ * skg_group_run -- enqueue the group on `stream`: x[i] bf16 [M, K[i]], W[i]
+ * bf16 [N[i], K[i]], residual[i] bf16 [M, N[i]] or NULL (the residual array
+ * itself may be NULL when no epilogue takes one), y[i] [M, N[i]] bf16 (fp32
+ * for SKG_EPI_FP32); x[i] and W[i] 16-byte aligned.  Allocates nothing.
+ * One run of a group may be in flight at a time.  After a device timeout
+ * (SKG_ERR_DEVICE_TIMEOUT from a later run or skg_group_check) the group's
+ * counters are inconsistent: destroy it.
+ */
+SKG_API skg_status skg_group_run(skg_group_t group, const void *const *x, const void *const *W,
+                                 const void *const *residual, void *const *y, void *stream);
+
+/* Launch shape: CTAs, ring stages, work units, and each projection's split (n ints). */
+SKG_API skg_status skg_group_info(skg_group_t group, int *grid, int *stages, int *units, int *split);
+
+/* Synchronize the group's last stream and report a device timeout, if any. */
+SKG_API skg_status skg_group_check(skg_group_t group);
+
+/* Free the group (after its work finished). */
+SKG_API skg_status skg_group_destroy(skg_group_t group);
+
 #ifdef __cplusplus
 }
 #endif

@@ -425,6 +425,19 @@ struct skg_plan_s {
     MapCache wmaps, xmaps;
 };
 
+// A group: several projections of the same M in one persistent launch.
+struct skg_group_s {
+    int n = 0, M = 0, m_pad = 0, device = 0, num_sms = 0, stages = 0, grid = 0, units = 0;
+    int N[kGroupMax] = {}, K[kGroupMax] = {}, epi[kGroupMax] = {}, dep[kGroupMax] = {};
+    int split[kGroupMax] = {}, n_tiles[kGroupMax] = {};
+    size_t ws_off[kGroupMax] = {}, ctr_off[kGroupMax] = {}, done_off = 0, ws_bytes = 0;
+    void *ws = nullptr;               // partials and counters of every projection, then done[]
+    unsigned int *err_host = nullptr; // mapped pinned word
+    unsigned int *err_dev = nullptr;
+    cudaStream_t last_stream = nullptr;
+    MapCache wmaps[kGroupMax], xmaps[kGroupMax];
+};
+
 namespace {
 
 skg_status ensure_workspace(skg_plan_s *p)
@@ -836,6 +849,198 @@ skg_status skg_plan_destroy(skg_plan_t p)
     if (p->err_host)
         cudaFreeHost(p->err_host);
     delete p;
+    return SKG_OK;
+}
+
+// --------------------------------------------------------------- groups
+skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilogue, const int *dep,
+                     skg_group_t *out)
+{
+    if (!out)
+        return fail(SKG_ERR_INVALID_ARG, "skg_group: out is NULL");
+    *out = nullptr;
+    if (n < 1 || n > kGroupMax)
+        return fail(SKG_ERR_UNSUPPORTED, "skg_group: n=%d outside 1..%d", n, kGroupMax);
+    if (!N || !K || !epilogue)
+        return fail(SKG_ERR_INVALID_ARG, "skg_group: N, K and epilogue must be non-NULL");
+    if (M < 3 || M > 64)
+        return fail(SKG_ERR_UNSUPPORTED, "skg_group: M=%d; groups run the split-K kernel (M = 3..64)", M);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    int major = 0, minor = 0, sms = 0, l2 = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+        return fail(SKG_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only",
+                    dev, major, minor);
+    skg_group_s *g = new (std::nothrow) skg_group_s();
+    if (!g)
+        return fail(SKG_ERR_CUDA, "out of host memory");
+    g->n = n;
+    g->M = M;
+    g->m_pad = (M + 15) / 16 * 16;
+    g->device = dev;
+    g->num_sms = sms;
+    size_t off = 0;
+    for (int i = 0; i < n; ++i) {
+        skg_plan_desc d;
+        const skg_status st = query(M, N[i], K[i], epilogue[i], sms, static_cast<size_t>(l2), &d);
+        if (st != SKG_OK) {
+            delete g;
+            return st;
+        }
+        g->N[i] = N[i];
+        g->K[i] = K[i];
+        g->epi[i] = epilogue[i];
+        g->dep[i] = (i > 0 && dep && dep[i]) ? 1 : 0;
+        // the picker's split for this projection, at most 8 (any split gives the same bits)
+        g->split[i] = std::min(8, d.split_k);
+        g->n_tiles[i] = (N[i] + kTileN - 1) / kTileN;
+        g->ws_off[i] = off;
+        off += (tc_partial_bytes(M, N[i], g->split[i]) + 255) / 256 * 256;
+        g->ctr_off[i] = off;
+        off += (static_cast<size_t>(g->n_tiles[i]) * sizeof(unsigned int) + 255) / 256 * 256;
+        g->units += g->n_tiles[i] * g->split[i];
+    }
+    g->done_off = off;
+    off += (kGroupMax + 1) * sizeof(unsigned int);
+    g->ws_bytes = off;
+    const int mp = g->m_pad;
+    g->stages = std::min(mp <= 16 ? 6 : (mp <= 48 ? 5 : 4), tc_max_stages(mp, 232448));
+    const int per_sm = group_ctas_per_sm(mp, g->stages);
+    if (per_sm < 1) {
+        delete g;
+        return fail(SKG_ERR_UNSUPPORTED, "skg_group: the group kernel cannot be resident at m_pad %d", mp);
+    }
+    // every CTA resident at once: a CTA waiting on a dependency only waits for running CTAs
+    g->grid = std::min(g->units, per_sm * sms);
+    e = cudaMalloc(&g->ws, g->ws_bytes);
+    if (e == cudaSuccess)
+        e = cudaMemset(g->ws, 0, g->ws_bytes);
+    if (e == cudaSuccess)
+        e = cudaHostAlloc(reinterpret_cast<void **>(&g->err_host), sizeof(unsigned int), cudaHostAllocMapped);
+    if (e == cudaSuccess) {
+        *g->err_host = 0;
+        e = cudaHostGetDevicePointer(reinterpret_cast<void **>(&g->err_dev), g->err_host, 0);
+    }
+    if (e != cudaSuccess) {
+        skg_group_destroy(g);
+        return cuda_fail(e, "skg_group allocation");
+    }
+    *out = g;
+    return SKG_OK;
+}
+
+skg_status skg_group_info(skg_group_t g, int *grid, int *stages, int *units, int *split)
+{
+    if (!g)
+        return fail(SKG_ERR_INVALID_ARG, "skg_group_info: group is NULL");
+    if (grid)
+        *grid = g->grid;
+    if (stages)
+        *stages = g->stages;
+    if (units)
+        *units = g->units;
+    if (split)
+        for (int i = 0; i < g->n; ++i)
+            split[i] = g->split[i];
+    return SKG_OK;
+}
+
+skg_status skg_group_run(skg_group_t g, const void *const *x, const void *const *W, const void *const *residual,
+                         void *const *y, void *stream)
+{
+    if (!g)
+        return fail(SKG_ERR_INVALID_ARG, "skg_group_run: group is NULL");
+    if (!x || !W || !y)
+        return fail(SKG_ERR_INVALID_ARG, "skg_group_run: x, W and y arrays must be non-NULL");
+    if (__atomic_load_n(g->err_host, __ATOMIC_ACQUIRE) != 0)
+        return fail(SKG_ERR_DEVICE_TIMEOUT, "an earlier launch of this group ran out of a bounded wait; "
+                    "destroy the group");
+    GroupParams gp;
+    memset(&gp, 0, sizeof(gp));
+    char *base = static_cast<char *>(g->ws);
+    int unit = 0;
+    for (int i = 0; i < g->n; ++i) {
+        const void *res = residual ? residual[i] : nullptr;
+        const bool want_res = g->epi[i] == SKG_EPI_BF16_RESIDUAL;
+        if (!x[i] || !W[i] || !y[i])
+            return fail(SKG_ERR_INVALID_ARG, "skg_group_run: projection %d: x, W and y must be non-NULL", i);
+        if (want_res != (res != nullptr))
+            return fail(SKG_ERR_INVALID_ARG, "skg_group_run: projection %d: residual %s", i,
+                        want_res ? "missing" : "given to an epilogue without one");
+        if (!aligned(x[i], 16) || !aligned(W[i], 16))
+            return fail(SKG_ERR_ALIGNMENT, "skg_group_run: projection %d: x and W must be 16-byte aligned", i);
+        if (!aligned(y[i], g->epi[i] == SKG_EPI_FP32 ? 4 : 2) || (res && !aligned(res, 2)))
+            return fail(SKG_ERR_ALIGNMENT, "skg_group_run: projection %d: y / residual miss their alignment", i);
+        const CUtensorMap *mw = nullptr, *mx = nullptr;
+        skg_status st = g->wmaps[i].get(W[i], g->N[i], g->K[i], kTileN, &mw);
+        if (st != SKG_OK)
+            return st;
+        st = g->xmaps[i].get(x[i], g->M, g->K[i], g->m_pad, &mx);
+        if (st != SKG_OK)
+            return st;
+        GroupProj &P = gp.proj[i];
+        P.tmW = *mw;
+        P.tmX = *mx;
+        P.res = static_cast<const uint16_t *>(res);
+        P.y = y[i];
+        P.ws = reinterpret_cast<float *>(base + g->ws_off[i]);
+        P.counters = reinterpret_cast<unsigned int *>(base + g->ctr_off[i]);
+        P.M = g->M;
+        P.N = g->N[i];
+        P.K = g->K[i];
+        P.nkb = (g->K[i] + kBlockK - 1) / kBlockK;
+        P.n_tiles = g->n_tiles[i];
+        P.split = g->split[i];
+        P.epilogue = g->epi[i];
+        P.dep = g->dep[i];
+        P.unit_begin = unit;
+        unit += g->n_tiles[i] * g->split[i];
+    }
+    gp.done = reinterpret_cast<unsigned int *>(base + g->done_off);
+    gp.err = g->err_dev;
+    gp.n = g->n;
+    gp.M = g->M;
+    gp.units = g->units;
+    gp.stages = g->stages;
+    gp.timeout_ns = kDefaultTimeoutNs;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = launch_group_tc(gp, g->m_pad, g->grid, true, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "skg_group_run launch");
+    g->last_stream = s;
+    return SKG_OK;
+}
+
+skg_status skg_group_check(skg_group_t g)
+{
+    if (!g)
+        return fail(SKG_ERR_INVALID_ARG, "skg_group_check: group is NULL");
+    cudaError_t e = g->last_stream ? cudaStreamSynchronize(g->last_stream) : cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "skg_group_check synchronize");
+    const unsigned w = __atomic_load_n(g->err_host, __ATOMIC_ACQUIRE);
+    if (w != 0)
+        return fail(SKG_ERR_DEVICE_TIMEOUT, "a launch of this group ran out of a bounded wait (bits 0x%x)", w);
+    return SKG_OK;
+}
+
+skg_status skg_group_destroy(skg_group_t g)
+{
+    if (!g)
+        return SKG_OK;
+    if (g->ws)
+        cudaFree(g->ws);
+    if (g->err_host)
+        cudaFreeHost(g->err_host);
+    delete g;
     return SKG_OK;
 }
 

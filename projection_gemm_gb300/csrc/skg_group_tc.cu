@@ -1,0 +1,500 @@
+// skg_group_tc.cu -- several projections of the same M in one persistent
+// split-K launch.
+//
+// The split-K kernel (skg_splitk_tc.cu) pays, per launch, the latency of its
+// first weight bytes and the tail of its last reductions; programmatic
+// dependent launch hides part of that between launches.  Here one launch
+// runs a list of projections: the work units (projection, 128-row tile,
+// split) are numbered projection by projection and CTA c takes units c,
+// c + grid, c + 2 grid, ... in that order.  The TMA ring, the two TMEM
+// accumulators and every barrier carry on from one unit to the next, so the
+// producer streams the next unit's weights while the epilogue still reduces
+// the previous one.  (The single-GPU analogue of fusing producer and
+// consumer in one kernel: "Hyper Optimizing Kimi K3 in vLLM: Moving Fast and
+// Responsibly", method details 2.)
+//
+// Dependencies: projection j with dep set reads its x (and residual) only
+// after every tile of projection j - 1 has been written.  The last CTA of a
+// tile adds one to done[j] (release) after its y stores; a producer that
+// reaches projection j requests that unit's first weight tiles, then waits
+// (bounded) until done[j - 1] covers all of its tiles (acquire), then loads
+// x.  CTAs take their units in order and the grid never exceeds what the
+// SMs hold at once, so a waiting CTA only waits for CTAs that are running.
+// The last CTA to finish the launch returns done[] to zero.
+//
+// Arithmetic: per unit exactly that of the one-projection kernel (canonical
+// chunks, the same tree, the same last-CTA reduction), so every projection's
+// output has the bits of skg_run at the same split.
+//
+// Ordering rule of the pages (background 2): weights may be requested before
+// griddepcontrol.wait or a dependency wait; x, residual, workspace, counters
+// and y only after.  Every wait is bounded; a timeout records an error bit,
+// raises the CTA's abort flag, drains the CTA's own copies and MMAs, and the
+// CTA frees its TMEM and returns (the group then reports the error and must
+// be destroyed: its counters are no longer consistent).
+#include <cuda_bf16.h>
+
+#include "skg_internal.h"
+#include "skg_ptx.cuh"
+
+namespace skg {
+namespace {
+
+#include "skg_tc_common.cuh"
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *ptr)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(unsigned *ptr, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(ptr), "r"(v) : "memory");
+}
+
+// Wait until *ctr >= target; false on timeout or when another role aborted.
+__device__ bool wait_counter(const unsigned *ctr, unsigned target, unsigned long long timeout_ns,
+                             volatile int *abort)
+{
+    if (ld_acquire_gpu(ctr) >= target)
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(128);
+        if (ld_acquire_gpu(ctr) >= target)
+            return true;
+        if (*abort)
+            return false;
+        if (globaltimer_ns() - t0 > timeout_ns)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void group_failure(const GroupParams &g, volatile int *abort, unsigned bit)
+{
+    *abort = 1;
+    if (g.err)
+        atomicOr(g.err, bit);
+}
+
+// Work unit u: projection j, its tile and split, and the split's k-blocks.
+struct Unit {
+    int j, tile, split, leaf0, present, kb_begin, nk;
+};
+
+__device__ __forceinline__ Unit unit_of(const GroupParams &g, int u)
+{
+    Unit r;
+    int j = 0;
+    while (j + 1 < g.n && u >= g.proj[j + 1].unit_begin)
+        ++j;
+    const GroupProj &P = g.proj[j];
+    const int local = u - P.unit_begin;
+    r.j = j;
+    r.tile = local % P.n_tiles;
+    r.split = local / P.n_tiles;
+    const int L = kChunks / P.split;
+    r.leaf0 = r.split * L;
+    r.present = max(0, min(L, chunks_present(P.nkb) - r.leaf0));
+    r.kb_begin = chunk_begin(r.leaf0, P.nkb);
+    r.nk = chunk_begin(r.leaf0 + r.present, P.nkb) - r.kb_begin;
+    return r;
+}
+
+template <int MPAD>
+__global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group_kernel(const __grid_constant__ GroupParams g)
+{
+    using Sh = TcShape<MPAD>;
+    constexpr int NC = Sh::kNC;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+
+    const int S = g.stages;
+    uint8_t *sW = smem;
+    uint8_t *sX = smem + S * kWBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sX + S * Sh::kXBytes);
+    uint64_t *empty = full + S;
+    uint64_t *tfull = empty + S;      // [2]
+    uint64_t *tempty = tfull + 2;     // [2]
+    uint64_t *drain = tempty + 2;     // [1]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort, [1] last
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int j = 0; j < g.n; ++j) {
+            tma_prefetch_desc(&g.proj[j].tmW);
+            tma_prefetch_desc(&g.proj[j].tmX);
+        }
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], kEpiThreads / 32);
+        }
+        mbar_init(drain, 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Sh::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            int it = 0;                   // ring stages issued so far (all units)
+            bool ok = true, grid_ready = false;
+            int x_ready = -1;             // projections <= x_ready may have x read
+            auto slot_free = [&](int k) {
+                return k < S || mbar_wait(&empty[k % S], ((k / S) & 1) ^ 1, g.timeout_ns, &flags[0]);
+            };
+            for (int u = blockIdx.x; u < g.units && ok; u += gridDim.x) {
+                const Unit U = unit_of(g, u);
+                if (U.nk == 0)
+                    continue;
+                const GroupProj &P = g.proj[U.j];
+                const int tile_row = U.tile * kTileN;
+                const int pre = U.nk < S ? U.nk : S;
+                // the first weight tiles need no wait (weights are static)
+                int armed = 0;
+                for (; armed < pre; ++armed) {
+                    if (!slot_free(it + armed))
+                        break;
+                    const int s = (it + armed) % S;
+                    mbar_arrive_expect_tx(&full[s], kWBytes + Sh::kXBytes);
+                    tma_load_2d(sW + s * kWBytes, &P.tmW, &full[s], (U.kb_begin + armed) * kBlockK, tile_row,
+                                pol_w);
+                }
+                if (armed < pre) {
+                    group_failure(g, &flags[0], kErrTimeoutProducer);
+                    it += armed;      // the drain below waits for these copies
+                    ok = false;
+                    break;
+                }
+                if (U.j > x_ready) {
+                    // x of this projection: after the previous grid, and after
+                    // the previous projection when the group says so
+                    if (!grid_ready) {
+                        pdl_wait();
+                        grid_ready = true;
+                    }
+                    if (P.dep && U.j > 0 &&
+                        !wait_counter(&g.done[U.j - 1], static_cast<unsigned>(g.proj[U.j - 1].n_tiles), g.timeout_ns,
+                                      &flags[0])) {
+                        group_failure(g, &flags[0], kErrTimeoutProducer);
+                        // the W copies above were issued: wait for them below
+                        it += pre;
+                        ok = false;
+                        break;
+                    }
+                    // the dependency's y stores are seen before these async-proxy reads
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    x_ready = U.j;
+                }
+                for (int i = 0; i < pre; ++i) {
+                    const int s = (it + i) % S;
+                    tma_load_2d(sX + s * Sh::kXBytes, &P.tmX, &full[s], (U.kb_begin + i) * kBlockK, 0, pol_x);
+                }
+                it += pre;
+                for (int i = pre; i < U.nk; ++i, ++it) {
+                    if (!slot_free(it)) {
+                        group_failure(g, &flags[0], kErrTimeoutProducer);
+                        ok = false;
+                        break;
+                    }
+                    const int s = it % S;
+                    mbar_arrive_expect_tx(&full[s], kWBytes + Sh::kXBytes);
+                    tma_load_2d(sW + s * kWBytes, &P.tmW, &full[s], (U.kb_begin + i) * kBlockK, tile_row, pol_w);
+                    tma_load_2d(sX + s * Sh::kXBytes, &P.tmX, &full[s], (U.kb_begin + i) * kBlockK, 0, pol_x);
+                }
+            }
+            if (flags[0]) {
+                // Abort: copies this thread issued land before the CTA exits.
+                // (A stage armed for W and x whose x never came cannot
+                // complete; its W bytes have landed once the wait times out.)
+                for (int s = 0; s < S && s < it; ++s) {
+                    const int last = s + S * ((it - 1 - s) / S);
+                    volatile int never = 0;
+                    mbar_wait(&full[s], (last / S) & 1, g.timeout_ns, &never);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            int it = 0;                   // ring stages consumed (all units)
+            int pc = 0;                   // chunks issued (all units): accumulator pc & 1
+            for (int u = blockIdx.x; u < g.units && ok; u += gridDim.x) {
+                const Unit U = unit_of(g, u);
+                const int nkb = g.proj[U.j].nkb;
+                for (int pl = 0; pl < U.present && ok; ++pl, ++pc) {
+                    const int b = pc & 1;
+                    const uint32_t q = static_cast<uint32_t>(pc >> 1);
+                    if (!mbar_wait(&tempty[b], (q & 1) ^ 1, g.timeout_ns, &flags[0])) {
+                        group_failure(g, &flags[0], kErrTimeoutMma);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(b * MPAD);
+                    const int kb0 = chunk_begin(U.leaf0 + pl, nkb);
+                    const int kb1 = chunk_begin(U.leaf0 + pl + 1, nkb);
+                    for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                        const int s = it % S;
+                        const uint32_t ph = (it / S) & 1;
+                        if (!mbar_wait(&full[s], ph, g.timeout_ns, &flags[0])) {
+                            group_failure(g, &flags[0], kErrTimeoutMma);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t ad = smem_desc_kmajor_sw128(smem_u32(sW + s * kWBytes));
+                        const uint64_t bd = smem_desc_kmajor_sw128(smem_u32(sX + s * Sh::kXBytes));
+#pragma unroll
+                        for (int kk = 0; kk < kBlockK / 16; ++kk)
+                            tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, Sh::kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        tc_commit(&empty[s]);
+                    }
+                    if (ok)
+                        tc_commit(&tfull[b]);
+                }
+            }
+            if (!ok) {
+                // Abort: wait for the MMAs already issued before TMEM is freed.
+                tc_commit(drain);
+                volatile int never = 0;
+                mbar_wait(drain, 0, g.timeout_ns, &never);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        pdl_wait();  // residual, workspace, counters and y only from here on
+        const int ew = warp - 2;
+        const int quarter = warp & 3;   // TMEM lanes this warp may access
+        const int half = ew >> 2;       // which half of the m_pad columns
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(half * NC);
+        const uint32_t lvl1 = lane_base + 2 * MPAD;
+        const uint32_t lvl2 = lane_base + 3 * MPAD;
+        int pc = 0;                     // chunks received (all units)
+        for (int u = blockIdx.x; u < g.units; u += gridDim.x) {
+            const Unit U = unit_of(g, u);
+            const GroupProj &P = g.proj[U.j];
+            float st0[NC], cur[NC];     // per unit: nothing lives across units
+            bool ok = true;
+            for (int pl = 0; pl < U.present; ++pl, ++pc) {
+                const int b = pc & 1;
+                const uint32_t q = static_cast<uint32_t>(pc >> 1);
+                if (!mbar_wait(&tfull[b], q & 1, g.timeout_ns, &flags[0])) {
+                    group_failure(g, &flags[0], kErrTimeoutEpilogue);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_load_cols<NC>(lane_base + static_cast<uint32_t>(b * MPAD), cur);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&tempty[b]);
+                // canonical tree over this unit's chunks (as in the one-projection kernel)
+                if (pl & 1) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) cur[c] = st0[c] + cur[c];
+                    if (pl & 2) {
+                        tmem_add_cols<NC>(lvl1, cur);
+                        if (pl & 4) {
+                            tmem_add_cols<NC>(lvl2, cur);
+                        } else {
+                            tmem_store_cols<NC>(lvl2, cur);
+                        }
+                    } else {
+                        tmem_store_cols<NC>(lvl1, cur);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) st0[c] = cur[c];
+                }
+            }
+            ok = epi_bar_and(ok && !flags[0]);
+            if (!ok)
+                break;
+            const int present = U.present;
+            if (present != 8 && present > 0) {
+                bool have = false;
+                if (present & 1) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) cur[c] = st0[c];
+                    have = true;
+                }
+                if (present & 2) {
+                    if (have) {
+                        tmem_add_cols<NC>(lvl1, cur);
+                    } else {
+                        tmem_load_cols<NC>(lvl1, cur);
+                    }
+                    have = true;
+                }
+                if (present & 4) {
+                    if (have) {
+                        tmem_add_cols<NC>(lvl2, cur);
+                    } else {
+                        tmem_load_cols<NC>(lvl2, cur);
+                    }
+                }
+            }
+            const int n = U.tile * kTileN + row;
+            if (present > 0 && n < P.N) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    const int m = half * NC + c;
+                    if (m < g.M)
+                        P.ws[((static_cast<size_t>(U.split) * P.n_tiles + U.tile) * P.M + m) * kTileN + row] = cur[c];
+                }
+            }
+            // Arrive on the tile's counter (see the one-projection kernel).
+            epi_bar_sync();
+            if (ew == 0 && lane == 0) {
+                const unsigned old = atom_add_acq_rel_gpu(&P.counters[U.tile], 1u);
+                flags[1] = (old == static_cast<unsigned>(P.split - 1)) ? 1 : 0;
+            }
+            epi_bar_sync();
+            if (flags[1]) {
+                const int L = kChunks / P.split;
+                const int sp = (chunks_present(P.nkb) + L - 1) / L;  // splits holding a value
+                if (P.dep && U.j > 0 && P.res) {
+                    // the residual may be the previous projection's output
+                    if (ew == 0 && lane == 0 &&
+                        !wait_counter(&g.done[U.j - 1], static_cast<unsigned>(g.proj[U.j - 1].n_tiles), g.timeout_ns,
+                                      &flags[0]))
+                        group_failure(g, &flags[0], kErrTimeoutEpilogue);
+                    if (!epi_bar_and(!flags[0]))
+                        break;
+                }
+                // splits are 2, 4 or 8 here (the group caps them; any split
+                // gives the same bits), 4 loads in flight per thread: the unit
+                // loop keeps more registers live than the one-projection kernel
+                const int et = threadIdx.x - 64;
+                switch (P.split) {
+                case 2: reduce_tile_v4<2, 4>(P, U.tile, sp, et); break;
+                case 4: reduce_tile_v4<4, 4>(P, U.tile, sp, et); break;
+                default: reduce_tile_v4<8, 4>(P, U.tile, sp, et); break;
+                }
+                // every y store of the tile comes before the release of done[j]
+                epi_bar_sync();
+                if (ew == 0 && lane == 0) {
+                    P.counters[U.tile] = 0;
+                    red_release_gpu_add(&g.done[U.j], 1u);
+                }
+            }
+        }
+    }
+
+    // Lanes that ran a role alone reconverge; then the last CTA of the grid
+    // returns the per-launch counters to zero (every CTA is past its waits).
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned old = atom_add_acq_rel_gpu(&g.done[kGroupMax], 1u);
+        if (old == gridDim.x - 1) {
+            for (int j = 0; j < g.n; ++j)
+                g.done[j] = 0;
+            g.done[kGroupMax] = 0;
+        }
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Sh::kTmemCols);
+    }
+}
+
+template <int MPAD>
+cudaError_t launch_group_t(const GroupParams &g, int grid, bool pdl, cudaStream_t s)
+{
+    const int smem = tc_smem_bytes(MPAD, g.stages);
+    static int attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&attr_set[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(splitk_group_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(splitk_group_kernel<MPAD>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
+        __atomic_store_n(&attr_set[dev], 1, __ATOMIC_RELEASE);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, splitk_group_kernel<MPAD>, g);
+}
+
+template <int MPAD>
+int ctas_per_sm_t(int stages)
+{
+    int n = 0;
+    if (cudaFuncSetAttribute(splitk_group_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_group_kernel<MPAD>, kTcThreads,
+                                                      tc_smem_bytes(MPAD, stages)) != cudaSuccess)
+        return 0;
+    const int by_tmem = 512 / tc_tmem_cols(MPAD);   // TMEM is not part of the occupancy query
+    return n < by_tmem ? n : by_tmem;
+}
+
+} // namespace
+
+cudaError_t launch_group_tc(const GroupParams &g, int m_pad, int grid, bool pdl, cudaStream_t s)
+{
+    switch (m_pad) {
+    case 16: return launch_group_t<16>(g, grid, pdl, s);
+    case 32: return launch_group_t<32>(g, grid, pdl, s);
+    case 48: return launch_group_t<48>(g, grid, pdl, s);
+    case 64: return launch_group_t<64>(g, grid, pdl, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int group_ctas_per_sm(int m_pad, int stages)
+{
+    switch (m_pad) {
+    case 16: return ctas_per_sm_t<16>(stages);
+    case 32: return ctas_per_sm_t<32>(stages);
+    case 48: return ctas_per_sm_t<48>(stages);
+    case 64: return ctas_per_sm_t<64>(stages);
+    default: return 0;
+    }
+}
+
+} // namespace skg

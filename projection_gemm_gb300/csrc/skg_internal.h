@@ -79,6 +79,28 @@ struct TcParams {
     unsigned long long timeout_ns;
 };
 
+// Several projections of the same M in one persistent split-K launch.
+constexpr int kGroupMax = 8;
+struct alignas(64) GroupProj {
+    CUtensorMap tmW;        // W [N, K], box 64 x 128
+    CUtensorMap tmX;        // x [M, K], box 64 x m_pad
+    const uint16_t *res;    // [M, N] bf16 bits or null
+    void *y;                // [M, N]
+    float *ws;              // fp32 partials, tile-major [split][tiles][M][128]
+    unsigned int *counters; // [n_tiles] arrival counters, zero between runs
+    int M, N, K, nkb, n_tiles, split, epilogue;
+    int dep;                // 1: x read only after the previous projection of the group is complete
+    int unit_begin;         // first work unit (tile, split) of this projection
+};
+
+struct GroupParams {
+    GroupProj proj[kGroupMax];
+    unsigned int *done;     // [kGroupMax] tiles finished per projection, [kGroupMax] CTAs finished
+    unsigned int *err;
+    int n, M, units, stages;
+    unsigned long long timeout_ns;
+};
+
 // The grid's share of an L2 prefetch of the next projection's weight: CTA
 // `cta` of `ctas` asks for its slice of [base, base + bytes), evict-last.
 __device__ __forceinline__ void prefetch_next_slice(const unsigned char *base, size_t bytes, unsigned cta,
@@ -136,6 +158,8 @@ cudaError_t gemv_occupancy(int M, int K, int split, int ring, int *ctas_per_sm);
 int gemv_strips_per_warp(int K, int split);   // must be <= 16
 cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p,
                              int m_pad, int grid, bool pdl, cudaStream_t s);
+cudaError_t launch_group_tc(const GroupParams &g, int m_pad, int grid, bool pdl, cudaStream_t s);
+int group_ctas_per_sm(int m_pad, int stages);   // co-resident CTAs of the group kernel
 // Clusters of `split` CTAs the tensor-core kernel can keep resident (0 if none).
 cudaError_t tc_max_active_clusters(int m_pad, int stages, int split, int grid, int *clusters);
 cudaError_t launch_prefetch_l2(const void *base, size_t bytes, cudaStream_t s);

@@ -37,6 +37,7 @@ EXPORTS = (
     "skg_prefetch_l2", "skg_plan_set_prefetch_fraction", "skg_plan_info", "skg_plan_check",
     "skg_plan_destroy", "skg_debug_wait_timeout", "skg_last_error", "skg_version",
     "skg_run_noalloc", "skg_plan_set_reduction", "skg_plan_set_l2_ahead", "skg_plan_set_next_weight",
+    "skg_group", "skg_group_run", "skg_group_info", "skg_group_check", "skg_group_destroy",
 )
 
 
@@ -93,6 +94,11 @@ def load(path: str = LIB_PATH):
     lib.skg_plan_set_reduction.argtypes = [vp, i]
     lib.skg_plan_set_l2_ahead.argtypes = [vp, i]
     lib.skg_plan_set_next_weight.argtypes = [vp, vp, sz]
+    lib.skg_group.argtypes = [i, i, P(i), P(i), P(i), P(i), P(vp)]
+    lib.skg_group_run.argtypes = [vp, P(vp), P(vp), P(vp), P(vp), vp]
+    lib.skg_group_info.argtypes = [vp, P(i), P(i), P(i), P(i)]
+    lib.skg_group_check.argtypes = [vp]
+    lib.skg_group_destroy.argtypes = [vp]
     for name in EXPORTS:
         getattr(lib, name).restype = ctypes.c_int
     lib.skg_last_error.restype = ctypes.c_char_p
@@ -243,6 +249,71 @@ class Plan:
     def close(self):
         if self.handle:
             skg_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------- groups
+def _ints(vals):
+    return (ctypes.c_int * len(vals))(*[int(v) for v in vals])
+
+
+def _ptrs(vals):
+    return (ctypes.c_void_p * len(vals))(*[_ptr(v) for v in vals])
+
+
+def skg_group(M: int, N, K, epilogue, dep=None) -> int:
+    g = ctypes.c_void_p()
+    n = len(N)
+    _check(load().skg_group(n, M, _ints(N), _ints(K), _ints([_epi(e) for e in epilogue]),
+                            _ints(dep) if dep is not None else None, ctypes.byref(g)))
+    return g.value
+
+
+def skg_group_run(group: int, x, W, residual, y, stream=None):
+    res = None if residual is None else _ptrs(residual)
+    _check(load().skg_group_run(group, _ptrs(x), _ptrs(W), res, _ptrs(y), _stream(stream)))
+
+
+def skg_group_info(group: int, n: int) -> dict:
+    grid, stages, units = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    split = (ctypes.c_int * n)()
+    _check(load().skg_group_info(group, ctypes.byref(grid), ctypes.byref(stages), ctypes.byref(units), split))
+    return {"grid": grid.value, "stages": stages.value, "units": units.value, "split": list(split)}
+
+
+def skg_group_check(group: int):
+    _check(load().skg_group_check(group))
+
+
+def skg_group_destroy(group: int):
+    _check(load().skg_group_destroy(group))
+
+
+class Group:
+    """Several projections of one M in one persistent launch (skg_group)."""
+
+    def __init__(self, M: int, N, K, epilogue, dep=None):
+        self.n = len(N)
+        self.handle = skg_group(M, N, K, epilogue, dep)
+
+    def run(self, x, W, residual, y, stream=None):
+        skg_group_run(self.handle, x, W, residual, y, stream)
+
+    def info(self) -> dict:
+        return skg_group_info(self.handle, self.n)
+
+    def check(self):
+        skg_group_check(self.handle)
+
+    def close(self):
+        if self.handle:
+            skg_group_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
