@@ -82,11 +82,14 @@ def kernel_source_hash(kernel: str) -> str:
     """sha256 of the CUDA source that defines `kernel` (its ncu counters are
     only valid for that exact source)."""
     import hashlib
-    src = {"splitk_tc": "skg_splitk_tc.cu", "gemv": "skg_gemv.cu"}.get(kernel)
-    if src is None:
+    srcs = {"splitk_tc": ("skg_splitk_tc.cu", "skg_tc_common.cuh"), "gemv": ("skg_gemv.cu",)}.get(kernel)
+    if srcs is None:
         return ""
-    with open(os.path.join(ROOT, "projection_gemm_gb300", "csrc", src), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    h = hashlib.sha256()
+    for src in srcs:
+        with open(os.path.join(ROOT, "projection_gemm_gb300", "csrc", src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def kernel_traffic(kernel: str, workload: str):
@@ -228,6 +231,40 @@ def host_data(projs):
     return out
 
 
+class GroupProjection:
+    """Several projections launched as one group: the bench's per-launch
+    figures (weight and algorithmic bytes, flops) summed over its members."""
+
+    def __init__(self, members):
+        self.members = members
+        self.M = members[0].M
+        self.N = [p.N for p in members]
+        self.K = [p.K for p in members]
+        self.name = f"{members[0].name}..{members[-1].name}"
+
+    def weight_bytes(self):
+        return sum(p.weight_bytes() for p in self.members)
+
+    def algorithmic_bytes(self):
+        return sum(p.algorithmic_bytes() for p in self.members)
+
+    def flops(self):
+        return sum(p.flops() for p in self.members)
+
+
+def make_group(members):
+    from projection_gemm_gb300 import skg
+    ps = [o["p"] for o in members]
+    g = skg.Group(ps[0].M, [p.N for p in ps], [p.K for p in ps], [p.epilogue for p in ps],
+                  [0] + [1] * (len(ps) - 1))
+    info = g.info()
+    return dict(p=GroupProjection(ps), group=g, plans=[o["plan"] for o in members],
+                info={"kernel": "splitk_group", "split_k": info["split"], "prefetch_bytes": 0,
+                      "grid": info["grid"], "stages": info["stages"]},
+                x=[o["x"] for o in members], W=[o["W"] for o in members], res=[o["res"] for o in members],
+                y=[o["y"] for o in members])
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -307,6 +344,20 @@ def run_ours(args):
             nxt = ops[(i + 1) % len(ops)]
             o["plan"].set_next_weight(nxt["W"], int(min(nxt["p"].weight_bytes(), next_frac * l2)))
 
+    # --fused: each run of consecutive projections with the same M >= 3 is
+    # one group launch (skg_group), every projection after the first ordered
+    # after the previous one (dep), as consecutive launches are.
+    if args.fused:
+        side_pf = False
+        segs, i = [], 0
+        while i < len(ops):
+            j = i + 1
+            while ops[i]["p"].M >= 3 and j < len(ops) and ops[j]["p"].M == ops[i]["p"].M:
+                j += 1
+            segs.append(ops[i] if j == i + 1 else make_group(ops[i:j]))
+            i = j
+        ops = segs
+
     # Runs of consecutive launches of one kernel kind: events at their
     # boundaries time each kind's launches without splitting the runs.
     groups, g0 = [], 0
@@ -316,6 +367,12 @@ def run_ours(args):
             g0 = i
     group_start = {a: j for j, (a, _) in enumerate(groups)}
 
+    def launch(o, s):
+        if "group" in o:
+            o["group"].run(o["x"], o["W"], o["res"], o["y"], s)
+        else:
+            o["plan"].run(o["x"], o["W"], o["res"], o["y"], s)
+
     def step(events=None, mode="launch", s=None):
         s = stream if s is None else s
         for i, o in enumerate(ops):
@@ -324,7 +381,7 @@ def run_ours(args):
                 ops[i + 1]["plan"].prefetch(ops[i + 1]["W"], side)
             if events is not None and (mode == "launch" or i in group_start):
                 events[i if mode == "launch" else group_start[i]].record(s)
-            o["plan"].run(o["x"], o["W"], o["res"], o["y"], s)
+            launch(o, s)
             if side_pf and i + 1 < len(ops):
                 s.wait_stream(side)
         if events is not None:
@@ -425,6 +482,8 @@ def run_ours(args):
         per_m[key] = {"M": p.M, "N": p.N, "K": p.K, "kernel": o["info"]["kernel"], "split": o["info"]["split_k"],
                       "us": round(us, 3), "weight_gbs": round(p.weight_bytes() / us / 1e3, 1),
                       "roofline_frac": round(t_ideal / us, 4)}
+        if "grid" in o["info"]:
+            per_m[key].update(grid=o["info"]["grid"], stages=o["info"]["stages"])
     dom = max(kern, key=lambda k: kern[k]["us"])
     achieved = kern[dom]["bytes"] / (kern[dom]["us"] * 1e-6) / 1e9
     traffic = kernel_traffic(dom, args.workload)
@@ -441,6 +500,7 @@ def run_ours(args):
         "config": {"workload": desc, **cfg, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": ("inputs larger than L2: every step streams %.1f MB of distinct weights" % (wbytes_step / 1e6)),
                    "pdl": bool(args.pdl),
+                   "fused_groups": bool(args.fused),
                    "launch": ("cuda graph of the step's launches, replayed (steps carrying events run eagerly)"
                               if graph is not None else "eager skg_run calls"),
                    "next_weight_l2_fraction": next_frac,
@@ -475,14 +535,19 @@ def run_ours(args):
                          "ms_per_step": round(te / Ke * 1e3, 4)}
 
     for o in ops:
-        o["plan"].check()
+        (o["group"] if "group" in o else o["plan"]).check()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(hostcopy, args.cpu_seconds)
         gbs, secs = smp.run()
         result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": smp.cores, "kind": "oracle",
                                   "sample": smp.desc, "seconds": round(secs, 2)}
     for o in ops:
-        o["plan"].close()
+        if "group" in o:
+            o["group"].close()
+            for pl in o["plans"]:
+                pl.close()
+        else:
+            o["plan"].close()
     if world > 1:
         dist.destroy_process_group()
     return result if rank == 0 else None
@@ -535,6 +600,8 @@ def main(argv=None):
     ap.add_argument("--next-weight", type=float, default=None,
                     help="fraction of L2 of the next projection's weight each launch asks the L2 for "
                          "(default: 0.15 for the chain, off otherwise)")
+    ap.add_argument("--fused", type=int, default=0,
+                    help="1: consecutive projections of one M >= 3 as one group launch (skg_group)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -429,7 +429,7 @@ struct skg_plan_s {
 struct skg_group_s {
     int n = 0, M = 0, m_pad = 0, device = 0, num_sms = 0, stages = 0, grid = 0, units = 0;
     int N[kGroupMax] = {}, K[kGroupMax] = {}, epi[kGroupMax] = {}, dep[kGroupMax] = {};
-    int split[kGroupMax] = {}, n_tiles[kGroupMax] = {};
+    int split[kGroupMax] = {}, n_tiles[kGroupMax] = {}, ahead[kGroupMax] = {};
     size_t ws_off[kGroupMax] = {}, ctr_off[kGroupMax] = {}, done_off = 0, ws_bytes = 0;
     void *ws = nullptr;               // partials and counters of every projection, then done[]
     unsigned int *err_host = nullptr; // mapped pinned word
@@ -901,6 +901,7 @@ skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilog
         g->dep[i] = (i > 0 && dep && dep[i]) ? 1 : 0;
         // the picker's split for this projection, at most 8 (any split gives the same bits)
         g->split[i] = std::min(8, d.split_k);
+        g->ahead[i] = d.l2_ahead;
         g->n_tiles[i] = (N[i] + kTileN - 1) / kTileN;
         g->ws_off[i] = off;
         off += (tc_partial_bytes(M, N[i], g->split[i]) + 255) / 256 * 256;
@@ -912,14 +913,34 @@ skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilog
     off += (kGroupMax + 1) * sizeof(unsigned int);
     g->ws_bytes = off;
     const int mp = g->m_pad;
-    g->stages = std::min(mp <= 16 ? 6 : (mp <= 48 ? 5 : 4), tc_max_stages(mp, 232448));
-    const int per_sm = group_ctas_per_sm(mp, g->stages);
+    // The most CTAs per SM that still keep a ring of 4 stages each, and the
+    // deepest ring at that count: while one CTA's epilogue reduces a tile the
+    // others keep the SM's weight stream going.
+    int per_sm = 0;
+    for (int s = tc_max_stages(mp, 232448); s >= 4; --s) {
+        const int c = group_ctas_per_sm(mp, s);
+        if (c > per_sm) {
+            per_sm = c;
+            g->stages = s;
+        }
+    }
     if (per_sm < 1) {
         delete g;
         return fail(SKG_ERR_UNSUPPORTED, "skg_group: the group kernel cannot be resident at m_pad %d", mp);
     }
-    // every CTA resident at once: a CTA waiting on a dependency only waits for running CTAs
-    g->grid = std::min(g->units, per_sm * sms);
+    // every CTA resident at once (a CTA waiting on a dependency only waits
+    // for running CTAs), and no more than the largest segment has units
+    int seg_max = 0;
+    for (int a = 0; a < n;) {
+        int b = a + 1, units = g->n_tiles[a] * g->split[a];
+        while (b < n && !g->dep[b]) {
+            units += g->n_tiles[b] * g->split[b];
+            ++b;
+        }
+        seg_max = std::max(seg_max, units);
+        a = b;
+    }
+    g->grid = std::min(seg_max, per_sm * sms);
     e = cudaMalloc(&g->ws, g->ws_bytes);
     if (e == cudaSuccess)
         e = cudaMemset(g->ws, 0, g->ws_bytes);
@@ -966,7 +987,6 @@ skg_status skg_group_run(skg_group_t g, const void *const *x, const void *const 
     GroupParams gp;
     memset(&gp, 0, sizeof(gp));
     char *base = static_cast<char *>(g->ws);
-    int unit = 0;
     for (int i = 0; i < g->n; ++i) {
         const void *res = residual ? residual[i] : nullptr;
         const bool want_res = g->epi[i] == SKG_EPI_BF16_RESIDUAL;
@@ -1001,8 +1021,23 @@ skg_status skg_group_run(skg_group_t g, const void *const *x, const void *const 
         P.split = g->split[i];
         P.epilogue = g->epi[i];
         P.dep = g->dep[i];
-        P.unit_begin = unit;
-        unit += g->n_tiles[i] * g->split[i];
+        P.ahead = g->ahead[i];
+    }
+    // segments: a projection with dep starts a new one
+    for (int a = 0; a < g->n;) {
+        int b = a + 1;
+        while (b < g->n && !g->dep[b])
+            ++b;
+        int units = 0;
+        for (int i = a; i < b; ++i) {
+            gp.proj[i].seg_begin = units;
+            units += g->n_tiles[i] * g->split[i];
+        }
+        for (int i = a; i < b; ++i) {
+            gp.proj[i].seg_units = units;
+            gp.proj[i].seg_next = b;
+        }
+        a = b;
     }
     gp.done = reinterpret_cast<unsigned int *>(base + g->done_off);
     gp.err = g->err_dev;

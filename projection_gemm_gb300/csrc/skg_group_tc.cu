@@ -4,9 +4,11 @@
 // The split-K kernel (skg_splitk_tc.cu) pays, per launch, the latency of its
 // first weight bytes and the tail of its last reductions; programmatic
 // dependent launch hides part of that between launches.  Here one launch
-// runs a list of projections: the work units (projection, 128-row tile,
-// split) are numbered projection by projection and CTA c takes units c,
-// c + grid, c + 2 grid, ... in that order.  The TMA ring, the two TMEM
+// runs a list of projections.  Projections joined without a dependency form
+// a segment; a segment's work units (projection, 128-row tile, split) are
+// numbered projection by projection and CTA c takes units c, c + grid, ...
+// of each segment, segment by segment -- so a projection that has to wait
+// for the previous one still spreads over the grid.  The TMA ring, the two TMEM
 // accumulators and every barrier carry on from one unit to the next, so the
 // producer streams the next unit's weights while the epilogue still reduces
 // the previous one.  (The single-GPU analogue of fusing producer and
@@ -33,6 +35,8 @@
 // CTA frees its TMEM and returns (the group then reports the error and must
 // be destroyed: its counters are no longer consistent).
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "skg_internal.h"
 #include "skg_ptx.cuh"
@@ -79,28 +83,57 @@ __device__ __forceinline__ void group_failure(const GroupParams &g, volatile int
         atomicOr(g.err, bit);
 }
 
-// Work unit u: projection j, its tile and split, and the split's k-blocks.
+// Work unit k of projection j: its tile and split, and the split's k-blocks.
 struct Unit {
     int j, tile, split, leaf0, present, kb_begin, nk;
 };
 
-__device__ __forceinline__ Unit unit_of(const GroupParams &g, int u)
+__device__ __forceinline__ Unit unit_at(const GroupParams &g, int j, int k)
 {
     Unit r;
-    int j = 0;
-    while (j + 1 < g.n && u >= g.proj[j + 1].unit_begin)
-        ++j;
     const GroupProj &P = g.proj[j];
-    const int local = u - P.unit_begin;
     r.j = j;
-    r.tile = local % P.n_tiles;
-    r.split = local / P.n_tiles;
+    r.tile = k % P.n_tiles;
+    r.split = k / P.n_tiles;
     const int L = kChunks / P.split;
     r.leaf0 = r.split * L;
     r.present = max(0, min(L, chunks_present(P.nkb) - r.leaf0));
     r.kb_begin = chunk_begin(r.leaf0, P.nkb);
     r.nk = chunk_begin(r.leaf0 + r.present, P.nkb) - r.kb_begin;
     return r;
+}
+
+// This CTA's units, in the order every role takes them: segment by segment,
+// within a segment the units v = blockIdx.x, blockIdx.x + grid, ...  Start
+// with j0 = 0, v = blockIdx.x.
+__device__ __forceinline__ bool next_unit(const GroupParams &g, int &j0, int &v, Unit &U)
+{
+    while (j0 < g.n) {
+        const GroupProj &S = g.proj[j0];
+        if (v < S.seg_units) {
+            int j = j0;
+            while (j + 1 < S.seg_next && v >= g.proj[j + 1].seg_begin)
+                ++j;
+            U = unit_at(g, j, v - g.proj[j].seg_begin);
+            v += gridDim.x;
+            return true;
+        }
+        j0 = S.seg_next;
+        v = blockIdx.x;
+    }
+    return false;
+}
+
+// The last CTA's reduction of a tile, as in the one-projection kernel, with
+// 8 loads in flight per thread (the unit loop keeps more registers live).
+template <int MPAD>
+__device__ __forceinline__ void group_reduce(const GroupProj *P, int tile, int sp, int et)
+{
+    switch (P->split) {
+    case 2: reduce_tile_v4<2, 4>(*P, tile, sp, et); break;
+    case 4: reduce_tile_v4<4, 4>(*P, tile, sp, et); break;
+    default: reduce_tile_v4<8, 4>(*P, tile, sp, et); break;
+    }
 }
 
 template <int MPAD>
@@ -165,8 +198,9 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
             auto slot_free = [&](int k) {
                 return k < S || mbar_wait(&empty[k % S], ((k / S) & 1) ^ 1, g.timeout_ns, &flags[0]);
             };
-            for (int u = blockIdx.x; u < g.units && ok; u += gridDim.x) {
-                const Unit U = unit_of(g, u);
+            int j0 = 0, v = blockIdx.x;
+            Unit U;
+            while (ok && next_unit(g, j0, v, U)) {
                 if (U.nk == 0)
                     continue;
                 const GroupProj &P = g.proj[U.j];
@@ -190,7 +224,10 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
                 }
                 if (U.j > x_ready) {
                     // x of this projection: after the previous grid, and after
-                    // the previous projection when the group says so
+                    // the previous projection when the group says so.  Until
+                    // then the W tiles past the ring stream into L2.
+                    for (int i = pre; i < U.nk && i < pre + P.ahead; ++i)
+                        tma_prefetch_l2_2d(&P.tmW, (U.kb_begin + i) * kBlockK, tile_row);
                     if (!grid_ready) {
                         pdl_wait();
                         grid_ready = true;
@@ -242,8 +279,9 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
             bool ok = true;
             int it = 0;                   // ring stages consumed (all units)
             int pc = 0;                   // chunks issued (all units): accumulator pc & 1
-            for (int u = blockIdx.x; u < g.units && ok; u += gridDim.x) {
-                const Unit U = unit_of(g, u);
+            int j0 = 0, v = blockIdx.x;
+            Unit U;
+            while (ok && next_unit(g, j0, v, U)) {
                 const int nkb = g.proj[U.j].nkb;
                 for (int pl = 0; pl < U.present && ok; ++pl, ++pc) {
                     const int b = pc & 1;
@@ -296,8 +334,9 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
         const uint32_t lvl1 = lane_base + 2 * MPAD;
         const uint32_t lvl2 = lane_base + 3 * MPAD;
         int pc = 0;                     // chunks received (all units)
-        for (int u = blockIdx.x; u < g.units; u += gridDim.x) {
-            const Unit U = unit_of(g, u);
+        int j0 = 0, v = blockIdx.x;
+        Unit U;
+        while (next_unit(g, j0, v, U)) {
             const GroupProj &P = g.proj[U.j];
             float st0[NC], cur[NC];     // per unit: nothing lives across units
             bool ok = true;
@@ -390,14 +429,8 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
                         break;
                 }
                 // splits are 2, 4 or 8 here (the group caps them; any split
-                // gives the same bits), 4 loads in flight per thread: the unit
-                // loop keeps more registers live than the one-projection kernel
-                const int et = threadIdx.x - 64;
-                switch (P.split) {
-                case 2: reduce_tile_v4<2, 4>(P, U.tile, sp, et); break;
-                case 4: reduce_tile_v4<4, 4>(P, U.tile, sp, et); break;
-                default: reduce_tile_v4<8, 4>(P, U.tile, sp, et); break;
-                }
+                // gives the same bits)
+                group_reduce<MPAD>(&P, U.tile, sp, threadIdx.x - 64);
                 // every y store of the tile comes before the release of done[j]
                 epi_bar_sync();
                 if (ew == 0 && lane == 0) {
@@ -460,17 +493,29 @@ cudaError_t launch_group_t(const GroupParams &g, int grid, bool pdl, cudaStream_
     return cudaLaunchKernelEx(&cfg, splitk_group_kernel<MPAD>, g);
 }
 
+// CTAs of the group kernel resident on one SM at once.  The runtime's
+// occupancy query answers 1 for every kernel that allocates tensor memory,
+// whatever its footprint, while such CTAs do share an SM (a kernel with 32
+// TMEM columns ran four CTAs per SM side by side); so the count is taken
+// from the kernel's own resources: the registers of its warps in each SM
+// sub-partition (ten warps put three on two of the four), shared memory with
+// the 1 KB the SM keeps per CTA, and TMEM columns.
 template <int MPAD>
 int ctas_per_sm_t(int stages)
 {
-    int n = 0;
-    if (cudaFuncSetAttribute(splitk_group_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_group_kernel<MPAD>, kTcThreads,
-                                                      tc_smem_bytes(MPAD, stages)) != cudaSuccess)
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, splitk_group_kernel<MPAD>) != cudaSuccess || a.numRegs <= 0)
         return 0;
-    const int by_tmem = 512 / tc_tmem_cols(MPAD);   // TMEM is not part of the occupancy query
-    return n < by_tmem ? n : by_tmem;
+    const int smem = tc_smem_bytes(MPAD, stages);
+    if (smem > 232448)
+        return 0;
+    const int warps_per_smsp = (kTcThreads / 32 + 3) / 4;
+    const int regs_per_warp = (a.numRegs * 32 + 255) / 256 * 256;
+    const int by_regs = 16384 / (warps_per_smsp * regs_per_warp);
+    const int by_smem = 233472 / (smem + 1024);
+    const int by_tmem = 512 / static_cast<int>(TcShape<MPAD>::kTmemCols);
+    const int by_threads = 2048 / kTcThreads;
+    return std::min(std::min(by_regs, by_smem), std::min(by_tmem, by_threads));
 }
 
 } // namespace

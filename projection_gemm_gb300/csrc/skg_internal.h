@@ -81,7 +81,7 @@ struct TcParams {
 
 // Several projections of the same M in one persistent split-K launch.
 constexpr int kGroupMax = 8;
-struct alignas(64) GroupProj {
+struct GroupProj {              // aligned as CUtensorMap
     CUtensorMap tmW;        // W [N, K], box 64 x 128
     CUtensorMap tmX;        // x [M, K], box 64 x m_pad
     const uint16_t *res;    // [M, N] bf16 bits or null
@@ -90,7 +90,14 @@ struct alignas(64) GroupProj {
     unsigned int *counters; // [n_tiles] arrival counters, zero between runs
     int M, N, K, nkb, n_tiles, split, epilogue;
     int dep;                // 1: x read only after the previous projection of the group is complete
-    int unit_begin;         // first work unit (tile, split) of this projection
+    int ahead;              // W k-blocks past the ring prefetched to L2 before a wait for x
+    // Segments: runs of projections joined without a dependency.  A
+    // segment's units (tile, split) are numbered projection by projection
+    // and dealt round-robin over the grid from CTA 0; CTAs take the segments
+    // in order.
+    int seg_begin;          // this projection's first unit within its segment
+    int seg_units;          // units of the whole segment
+    int seg_next;           // first projection after the segment
 };
 
 struct GroupParams {
