@@ -245,10 +245,9 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
             const int mp = (M + 15) / 16 * 16;
             stages = mp <= 16 ? 6 : (mp <= 48 ? 5 : 4);
             stages = std::min(stages, tc_max_stages(mp, 232448));
-            const int slots = num_sms * tc_ctas_per_sm(mp, stages);
             d->l2_ahead = 2;   // measured: 2-4 tiles after the ring into L2 before the wait
             split = 2;
-            while (split < kChunks && n_tiles * split * 2 <= std::min(slots, num_sms * 8 / 5))
+            while (split < kChunks && n_tiles * split * 2 <= num_sms * 8 / 5)
                 split *= 2;
         }
         fill_tc(d, split, stages, burst);

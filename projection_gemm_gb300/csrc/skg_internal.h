@@ -156,7 +156,6 @@ int gemv_span_grid(int M, int N, int K, int batch_strips, int num_sms);
 constexpr int kGemvMaxSmem = 226 * 1024;      // x (M * K * 2 bytes) + the weight rings (static smem needs the rest)
 int tc_max_stages(int m_pad, int smem_limit);
 int tc_tmem_cols(int m_pad);                  // TMEM columns one CTA allocates
-int tc_ctas_per_sm(int m_pad, int stages);    // co-resident CTAs (registers, shared memory, TMEM)
 constexpr int kTcDefaultStages = 4;
 
 // Launchers (return the cudaError_t of the launch).

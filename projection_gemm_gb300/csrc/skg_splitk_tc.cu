@@ -472,16 +472,6 @@ int tc_tmem_cols(int m_pad)
     return c;
 }
 
-int tc_ctas_per_sm(int m_pad, int stages)
-{
-    const int by_smem = 233472 / (tc_smem_bytes(m_pad, stages) + 1024);   // 228 KB per SM, 1 KB reserved per CTA
-    const int by_regs = m_pad <= 32 ? 3 : 2;                               // the kernel's launch bounds
-    const int by_tmem = 512 / tc_tmem_cols(m_pad);
-    int n = by_smem < by_regs ? by_smem : by_regs;
-    n = n < by_tmem ? n : by_tmem;
-    return n < 1 ? 1 : n;
-}
-
 int tc_max_stages(int m_pad, int smem_limit)
 {
     int s = 16;
