@@ -295,7 +295,8 @@ SKG_API int skg_version(void);
  * Groups -- several projections of the same M (3..64) in one persistent
  * split-K launch.  [OC] fuses producer and consumer in one kernel across
  * GPUs; this is the one-GPU form of that idea: the launch's CTAs take the
- * work units (projection, 128-row tile, split) in projection order, keep
+ * work units (projection, 128-row tile, split) from a counter in projection
+ * order (so the launch completes with any part of its grid resident), keep
  * their TMA ring, TMEM and barriers from one unit to the next, and stream
  * the next projection's weights while the previous one is still being
  * reduced, so consecutive projections pay no launch head or tail between

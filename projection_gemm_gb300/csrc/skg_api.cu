@@ -909,7 +909,7 @@ skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilog
         g->units += g->n_tiles[i] * g->split[i];
     }
     g->done_off = off;
-    off += (kGroupMax + 1) * sizeof(unsigned int);
+    off += kGroupDoneWords * sizeof(unsigned int);
     g->ws_bytes = off;
     const int mp = g->m_pad;
     // The most CTAs per SM that still keep a ring of 4 stages each, and the
@@ -927,19 +927,9 @@ skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilog
         delete g;
         return fail(SKG_ERR_UNSUPPORTED, "skg_group: the group kernel cannot be resident at m_pad %d", mp);
     }
-    // every CTA resident at once (a CTA waiting on a dependency only waits
-    // for running CTAs), and no more than the largest segment has units
-    int seg_max = 0;
-    for (int a = 0; a < n;) {
-        int b = a + 1, units = g->n_tiles[a] * g->split[a];
-        while (b < n && !g->dep[b]) {
-            units += g->n_tiles[b] * g->split[b];
-            ++b;
-        }
-        seg_max = std::max(seg_max, units);
-        a = b;
-    }
-    g->grid = std::min(seg_max, per_sm * sms);
+    // one wave: CTAs beyond the SMs' capacity would only start once others
+    // finished (correct -- units are handed out in order -- but idle)
+    g->grid = std::min(g->units, per_sm * sms);
     e = cudaMalloc(&g->ws, g->ws_bytes);
     if (e == cudaSuccess)
         e = cudaMemset(g->ws, 0, g->ws_bytes);
@@ -980,12 +970,13 @@ skg_status skg_group_run(skg_group_t g, const void *const *x, const void *const 
         return fail(SKG_ERR_INVALID_ARG, "skg_group_run: group is NULL");
     if (!x || !W || !y)
         return fail(SKG_ERR_INVALID_ARG, "skg_group_run: x, W and y arrays must be non-NULL");
-    if (__atomic_load_n(g->err_host, __ATOMIC_ACQUIRE) != 0)
-        return fail(SKG_ERR_DEVICE_TIMEOUT, "an earlier launch of this group ran out of a bounded wait; "
-                    "destroy the group");
+    if (const unsigned w = __atomic_load_n(g->err_host, __ATOMIC_ACQUIRE))
+        return fail(SKG_ERR_DEVICE_TIMEOUT, "an earlier launch of this group ran out of a bounded wait (bits 0x%x); "
+                    "destroy the group", w);
     GroupParams gp;
     memset(&gp, 0, sizeof(gp));
     char *base = static_cast<char *>(g->ws);
+    int unit = 0;
     for (int i = 0; i < g->n; ++i) {
         const void *res = residual ? residual[i] : nullptr;
         const bool want_res = g->epi[i] == SKG_EPI_BF16_RESIDUAL;
@@ -1021,22 +1012,8 @@ skg_status skg_group_run(skg_group_t g, const void *const *x, const void *const 
         P.epilogue = g->epi[i];
         P.dep = g->dep[i];
         P.ahead = g->ahead[i];
-    }
-    // segments: a projection with dep starts a new one
-    for (int a = 0; a < g->n;) {
-        int b = a + 1;
-        while (b < g->n && !g->dep[b])
-            ++b;
-        int units = 0;
-        for (int i = a; i < b; ++i) {
-            gp.proj[i].seg_begin = units;
-            units += g->n_tiles[i] * g->split[i];
-        }
-        for (int i = a; i < b; ++i) {
-            gp.proj[i].seg_units = units;
-            gp.proj[i].seg_next = b;
-        }
-        a = b;
+        P.unit_begin = unit;
+        unit += g->n_tiles[i] * g->split[i];
     }
     gp.done = reinterpret_cast<unsigned int *>(base + g->done_off);
     gp.err = g->err_dev;

@@ -4,36 +4,39 @@
 // The split-K kernel (skg_splitk_tc.cu) pays, per launch, the latency of its
 // first weight bytes and the tail of its last reductions; programmatic
 // dependent launch hides part of that between launches.  Here one launch
-// runs a list of projections.  Projections joined without a dependency form
-// a segment; a segment's work units (projection, 128-row tile, split) are
-// numbered projection by projection and CTA c takes units c, c + grid, ...
-// of each segment, segment by segment -- so a projection that has to wait
-// for the previous one still spreads over the grid.  The TMA ring, the two TMEM
-// accumulators and every barrier carry on from one unit to the next, so the
-// producer streams the next unit's weights while the epilogue still reduces
-// the previous one.  (The single-GPU analogue of fusing producer and
-// consumer in one kernel: "Hyper Optimizing Kimi K3 in vLLM: Moving Fast and
-// Responsibly", method details 2.)
+// runs a list of projections.  The work units (projection, 128-row tile,
+// split) are numbered projection by projection, and a CTA takes the next
+// unit from a global counter whenever its producer is ready for one.  The
+// TMA ring, the two TMEM accumulators and every barrier carry on from one
+// unit to the next, so the producer streams the next unit's weights while
+// the epilogue still reduces the previous one.  (The single-GPU analogue of
+// fusing producer and consumer in one kernel: "Hyper Optimizing Kimi K3 in
+// vLLM: Moving Fast and Responsibly", method details 2.)
 //
 // Dependencies: projection j with dep set reads its x (and residual) only
 // after every tile of projection j - 1 has been written.  The last CTA of a
-// tile adds one to done[j] (release) after its y stores; a producer that
-// reaches projection j requests that unit's first weight tiles, then waits
+// tile adds one to done[j] (release) after its y stores; a producer holding
+// a unit of projection j requests its first weight tiles, then waits
 // (bounded) until done[j - 1] covers all of its tiles (acquire), then loads
-// x.  CTAs take their units in order and the grid never exceeds what the
-// SMs hold at once, so a waiting CTA only waits for CTAs that are running.
-// The last CTA to finish the launch returns done[] to zero.
+// x.  Units are handed out in projection order, so every unit of projection
+// j - 1 already belongs to a running CTA, and that CTA waits on nothing
+// later: the launch completes whatever part of the grid is resident.  (A
+// fixed assignment of units to CTAs would need the whole grid resident at
+// once, which kernels still running on the SMs can prevent.)  The last CTA
+// to finish returns done[] and the unit counter to zero.
 //
 // Arithmetic: per unit exactly that of the one-projection kernel (canonical
 // chunks, the same tree, the same last-CTA reduction), so every projection's
-// output has the bits of skg_run at the same split.
+// output has the bits of skg_run at the same split, whichever CTA ran which
+// unit.
 //
 // Ordering rule of the pages (background 2): weights may be requested before
-// griddepcontrol.wait or a dependency wait; x, residual, workspace, counters
-// and y only after.  Every wait is bounded; a timeout records an error bit,
-// raises the CTA's abort flag, drains the CTA's own copies and MMAs, and the
-// CTA frees its TMEM and returns (the group then reports the error and must
-// be destroyed: its counters are no longer consistent).
+// griddepcontrol.wait or a dependency wait; the unit counter, x, residual,
+// workspace, counters and y only after.  Every wait is bounded; a timeout
+// records an error bit, raises the CTA's abort flag, drains the CTA's own
+// copies and MMAs, and the CTA frees its TMEM and returns (the group then
+// reports the error and must be destroyed: its counters are no longer
+// consistent).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -103,29 +106,18 @@ __device__ __forceinline__ Unit unit_at(const GroupParams &g, int j, int k)
     return r;
 }
 
-// This CTA's units, in the order every role takes them: segment by segment,
-// within a segment the units v = blockIdx.x, blockIdx.x + grid, ...  Start
-// with j0 = 0, v = blockIdx.x.
-__device__ __forceinline__ bool next_unit(const GroupParams &g, int &j0, int &v, Unit &U)
+// Unit u of the launch (projection by projection).
+__device__ __forceinline__ Unit unit_of(const GroupParams &g, int u)
 {
-    while (j0 < g.n) {
-        const GroupProj &S = g.proj[j0];
-        if (v < S.seg_units) {
-            int j = j0;
-            while (j + 1 < S.seg_next && v >= g.proj[j + 1].seg_begin)
-                ++j;
-            U = unit_at(g, j, v - g.proj[j].seg_begin);
-            v += gridDim.x;
-            return true;
-        }
-        j0 = S.seg_next;
-        v = blockIdx.x;
-    }
-    return false;
+    int j = 0;
+    while (j + 1 < g.n && u >= g.proj[j + 1].unit_begin)
+        ++j;
+    return unit_at(g, j, u - g.proj[j].unit_begin);
 }
 
 // The last CTA's reduction of a tile, as in the one-projection kernel, with
-// 8 loads in flight per thread (the unit loop keeps more registers live).
+// 4 loads in flight per thread (the unit loop keeps more registers live;
+// 8 or 16, as there, measured slower here).
 template <int MPAD>
 __device__ __forceinline__ void group_reduce(const GroupProj *P, int tile, int sp, int et)
 {
@@ -154,8 +146,12 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
     uint64_t *tfull = empty + S;      // [2]
     uint64_t *tempty = tfull + 2;     // [2]
     uint64_t *drain = tempty + 2;     // [1]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    constexpr int Q = kGroupUnitQueue;
+    uint64_t *uq_full = drain + 1;    // [Q] unit id written (producer)
+    uint64_t *uq_empty = uq_full + Q; // [Q] unit id read (MMA and epilogue)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(uq_empty + Q);
     volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort, [1] last
+    volatile int *uq = flags + 2;     // [Q] unit ids, -1 = no more units
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -173,6 +169,10 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
             mbar_init(&tempty[b], kEpiThreads / 32);
         }
         mbar_init(drain, 1);
+        for (int i = 0; i < Q; ++i) {
+            mbar_init(&uq_full[i], 1);
+            mbar_init(&uq_empty[i], 2);
+        }
         flags[0] = 0;
         flags[1] = 0;
         fence_mbar_init();
@@ -193,14 +193,34 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
             int it = 0;                   // ring stages issued so far (all units)
-            bool ok = true, grid_ready = false;
-            int x_ready = -1;             // projections <= x_ready may have x read
+            bool ok = true;
+            int x_ready = 0;              // projections < x_ready may have x read
             auto slot_free = [&](int k) {
                 return k < S || mbar_wait(&empty[k % S], ((k / S) & 1) ^ 1, g.timeout_ns, &flags[0]);
             };
-            int j0 = 0, v = blockIdx.x;
-            Unit U;
-            while (ok && next_unit(g, j0, v, U)) {
+            // Until the previous grid completes, warm L2 with the first
+            // weight tiles of unit blockIdx.x: the first units handed out
+            // are 0 .. grid - 1, in whatever order the CTAs arrive.
+            if (static_cast<int>(blockIdx.x) < g.units) {
+                const Unit U0 = unit_of(g, blockIdx.x);
+                const GroupProj &P0 = g.proj[U0.j];
+                for (int i = 0; i < U0.nk && i < S + P0.ahead; ++i)
+                    tma_prefetch_l2_2d(&P0.tmW, (U0.kb_begin + i) * kBlockK, U0.tile * kTileN);
+            }
+            pdl_wait();   // the unit counter and x only from here on
+            for (int q = 0; ok; ++q) {
+                if (q >= Q && !mbar_wait(&uq_empty[q % Q], ((q / Q) & 1) ^ 1, g.timeout_ns, &flags[0])) {
+                    group_failure(g, &flags[0], kErrTimeoutProducer);
+                    ok = false;
+                    break;
+                }
+                const unsigned u = atomicAdd(&g.done[kGroupDoneNext], 1u);
+                const bool last = u >= static_cast<unsigned>(g.units);
+                uq[q % Q] = last ? -1 : static_cast<int>(u);
+                mbar_arrive(&uq_full[q % Q]);
+                if (last)
+                    break;
+                const Unit U = unit_of(g, static_cast<int>(u));
                 if (U.nk == 0)
                     continue;
                 const GroupProj &P = g.proj[U.j];
@@ -222,28 +242,25 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
                     ok = false;
                     break;
                 }
-                if (U.j > x_ready) {
-                    // x of this projection: after the previous grid, and after
-                    // the previous projection when the group says so.  Until
-                    // then the W tiles past the ring stream into L2.
-                    for (int i = pre; i < U.nk && i < pre + P.ahead; ++i)
-                        tma_prefetch_l2_2d(&P.tmW, (U.kb_begin + i) * kBlockK, tile_row);
-                    if (!grid_ready) {
-                        pdl_wait();
-                        grid_ready = true;
-                    }
-                    if (P.dep && U.j > 0 &&
-                        !wait_counter(&g.done[U.j - 1], static_cast<unsigned>(g.proj[U.j - 1].n_tiles), g.timeout_ns,
-                                      &flags[0])) {
-                        group_failure(g, &flags[0], kErrTimeoutProducer);
-                        // the W copies above were issued: wait for them below
-                        it += pre;
-                        ok = false;
-                        break;
+                if (U.j >= x_ready) {
+                    // x of this projection: after the previous projection
+                    // when the group says so.  Until then the W tiles past
+                    // the ring stream into L2.
+                    if (P.dep && U.j > 0) {
+                        for (int i = pre; i < U.nk && i < pre + P.ahead; ++i)
+                            tma_prefetch_l2_2d(&P.tmW, (U.kb_begin + i) * kBlockK, tile_row);
+                        if (!wait_counter(&g.done[U.j - 1], static_cast<unsigned>(g.proj[U.j - 1].n_tiles),
+                                          g.timeout_ns, &flags[0])) {
+                            group_failure(g, &flags[0], kErrTimeoutProducer);
+                            // the W copies above were issued: wait for them below
+                            it += pre;
+                            ok = false;
+                            break;
+                        }
                     }
                     // the dependency's y stores are seen before these async-proxy reads
                     asm volatile("fence.proxy.async.global;" ::: "memory");
-                    x_ready = U.j;
+                    x_ready = U.j + 1;
                 }
                 for (int i = 0; i < pre; ++i) {
                     const int s = (it + i) % S;
@@ -279,9 +296,17 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
             bool ok = true;
             int it = 0;                   // ring stages consumed (all units)
             int pc = 0;                   // chunks issued (all units): accumulator pc & 1
-            int j0 = 0, v = blockIdx.x;
-            Unit U;
-            while (ok && next_unit(g, j0, v, U)) {
+            for (int qi = 0; ok; ++qi) {
+                if (!mbar_wait(&uq_full[qi % Q], (qi / Q) & 1, g.timeout_ns, &flags[0])) {
+                    group_failure(g, &flags[0], kErrTimeoutMma);
+                    ok = false;
+                    break;
+                }
+                const int u = uq[qi % Q];
+                mbar_arrive(&uq_empty[qi % Q]);
+                if (u < 0)
+                    break;
+                const Unit U = unit_of(g, u);
                 const int nkb = g.proj[U.j].nkb;
                 for (int pl = 0; pl < U.present && ok; ++pl, ++pc) {
                     const int b = pc & 1;
@@ -334,9 +359,19 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
         const uint32_t lvl1 = lane_base + 2 * MPAD;
         const uint32_t lvl2 = lane_base + 3 * MPAD;
         int pc = 0;                     // chunks received (all units)
-        int j0 = 0, v = blockIdx.x;
-        Unit U;
-        while (next_unit(g, j0, v, U)) {
+        for (int qi = 0;; ++qi) {
+            const bool got = mbar_wait(&uq_full[qi % Q], (qi / Q) & 1, g.timeout_ns, &flags[0]);
+            if (!got)
+                group_failure(g, &flags[0], kErrTimeoutEpilogue);
+            const int u = got ? uq[qi % Q] : -1;
+            // every epilogue thread holds the unit id before the slot is released
+            if (!epi_bar_and(got))
+                break;
+            if (ew == 0 && lane == 0)
+                mbar_arrive(&uq_empty[qi % Q]);
+            if (u < 0)
+                break;
+            const Unit U = unit_of(g, u);
             const GroupProj &P = g.proj[U.j];
             float st0[NC], cur[NC];     // per unit: nothing lives across units
             bool ok = true;
@@ -447,11 +482,12 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned old = atom_add_acq_rel_gpu(&g.done[kGroupMax], 1u);
+        const unsigned old = atom_add_acq_rel_gpu(&g.done[kGroupDoneExit], 1u);
         if (old == gridDim.x - 1) {
             for (int j = 0; j < g.n; ++j)
                 g.done[j] = 0;
-            g.done[kGroupMax] = 0;
+            g.done[kGroupDoneNext] = 0;
+            g.done[kGroupDoneExit] = 0;
         }
     }
     if (warp == 1) {
@@ -463,7 +499,7 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
 template <int MPAD>
 cudaError_t launch_group_t(const GroupParams &g, int grid, bool pdl, cudaStream_t s)
 {
-    const int smem = tc_smem_bytes(MPAD, g.stages);
+    const int smem = group_smem_bytes(MPAD, g.stages);
     static int attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -497,21 +533,20 @@ cudaError_t launch_group_t(const GroupParams &g, int grid, bool pdl, cudaStream_
 // occupancy query answers 1 for every kernel that allocates tensor memory,
 // whatever its footprint, while such CTAs do share an SM (a kernel with 32
 // TMEM columns ran four CTAs per SM side by side); so the count is taken
-// from the kernel's own resources: the registers of its warps in each SM
-// sub-partition (ten warps put three on two of the four), shared memory with
-// the 1 KB the SM keeps per CTA, and TMEM columns.
+// from the kernel's own resources: registers (each of the four SM
+// sub-partitions holds 16K, whole warps each), shared memory with the 1 KB
+// the SM keeps per CTA, TMEM columns and threads.
 template <int MPAD>
 int ctas_per_sm_t(int stages)
 {
     cudaFuncAttributes a;
     if (cudaFuncGetAttributes(&a, splitk_group_kernel<MPAD>) != cudaSuccess || a.numRegs <= 0)
         return 0;
-    const int smem = tc_smem_bytes(MPAD, stages);
+    const int smem = group_smem_bytes(MPAD, stages);
     if (smem > 232448)
         return 0;
-    const int warps_per_smsp = (kTcThreads / 32 + 3) / 4;
     const int regs_per_warp = (a.numRegs * 32 + 255) / 256 * 256;
-    const int by_regs = 16384 / (warps_per_smsp * regs_per_warp);
+    const int by_regs = 4 * (16384 / regs_per_warp) / (kTcThreads / 32);
     const int by_smem = 233472 / (smem + 1024);
     const int by_tmem = 512 / static_cast<int>(TcShape<MPAD>::kTmemCols);
     const int by_threads = 2048 / kTcThreads;
@@ -519,6 +554,13 @@ int ctas_per_sm_t(int stages)
 }
 
 } // namespace
+
+int group_smem_bytes(int m_pad, int stages)
+{
+    // the one-projection kernel's layout, then the unit queue: Q x (two
+    // barriers + one id)
+    return tc_smem_bytes(m_pad, stages) + kGroupUnitQueue * (2 * 8 + 4);
+}
 
 cudaError_t launch_group_tc(const GroupParams &g, int m_pad, int grid, bool pdl, cudaStream_t s)
 {

@@ -91,18 +91,19 @@ struct GroupProj {              // aligned as CUtensorMap
     int M, N, K, nkb, n_tiles, split, epilogue;
     int dep;                // 1: x read only after the previous projection of the group is complete
     int ahead;              // W k-blocks past the ring prefetched to L2 before a wait for x
-    // Segments: runs of projections joined without a dependency.  A
-    // segment's units (tile, split) are numbered projection by projection
-    // and dealt round-robin over the grid from CTA 0; CTAs take the segments
-    // in order.
-    int seg_begin;          // this projection's first unit within its segment
-    int seg_units;          // units of the whole segment
-    int seg_next;           // first projection after the segment
+    int unit_begin;         // first work unit (tile, split) of this projection
 };
+
+constexpr int kGroupDoneExit = kGroupMax;
+constexpr int kGroupDoneNext = kGroupMax + 1;
+constexpr int kGroupDoneWords = kGroupMax + 2;
+constexpr int kGroupUnitQueue = 16;   // unit ids in flight from the producer to the MMA and epilogue
+int group_smem_bytes(int m_pad, int stages);
 
 struct GroupParams {
     GroupProj proj[kGroupMax];
-    unsigned int *done;     // [kGroupMax] tiles finished per projection, [kGroupMax] CTAs finished
+    unsigned int *done;     // [j < kGroupMax] tiles finished per projection, [kGroupDoneExit] CTAs
+                            // finished, [kGroupDoneNext] units handed out
     unsigned int *err;
     int n, M, units, stages;
     unsigned long long timeout_ns;
