@@ -403,7 +403,7 @@ def run_ours(args):
     # projection) and replayed each step, so the host issues one launch per
     # step.  Steps that carry events run eagerly.
     graph = None
-    if args.graph:
+    if args.graph or (args.e2e_launch == "graph" and not args.no_e2e):
         cap = torch.cuda.Stream(device=dev)
         cap.wait_stream(stream)
         with torch.cuda.stream(cap):
@@ -442,7 +442,7 @@ def run_ours(args):
     w0 = time.time()
     start.record(stream)
     for k in range(K):
-        if graph is not None and k not in evs:
+        if args.graph and k not in evs:
             graph.replay()
         else:
             step(evs.get(k), modes.get(k, "launch"))
@@ -502,7 +502,7 @@ def run_ours(args):
                    "pdl": bool(args.pdl),
                    "fused_groups": bool(args.fused),
                    "launch": ("cuda graph of the step's launches, replayed (steps carrying events run eagerly)"
-                              if graph is not None else "eager skg_run calls"),
+                              if args.graph else "eager skg_run calls"),
                    "next_weight_l2_fraction": next_frac,
                    "side_stream_prefetch_fraction": args.prefetch if side_pf else 0.0},
         "per_projection": per_m, "roofline": roofline,
@@ -518,7 +518,10 @@ def run_ours(args):
 
         def e2e_step():
             dev_in.copy_(host_in, non_blocking=True)
-            step()
+            if args.e2e_launch == "graph":
+                graph.replay()
+            else:
+                step()
             host_out.copy_(dev_out, non_blocking=True)
             stream.synchronize()
         for _ in range(2):
@@ -532,7 +535,11 @@ def run_ours(args):
         te, eb = aggregate(te, wbytes_step * Ke, world)
         result["e2e"] = {"value": round(eb / te / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h, "steps": Ke,
-                         "ms_per_step": round(te / Ke * 1e3, 4)}
+                         "ms_per_step": round(te / Ke * 1e3, 4),
+                         "launch": ("each step's skg_run calls captured once as a CUDA graph and replayed "
+                                    "between the copies" if args.e2e_launch == "graph" else
+                                    "eager skg_run calls between the copies"),
+                         "sync": "host waits for every step's output copy before the next step"}
 
     for o in ops:
         (o["group"] if "group" in o else o["plan"]).check()
@@ -595,6 +602,8 @@ def main(argv=None):
     ap.add_argument("--pdl", type=int, default=1)
     ap.add_argument("--graph", type=int, default=0,
                     help="1: replay each step as one captured CUDA graph (measured slower: replays do not overlap)")
+    ap.add_argument("--e2e-launch", choices=("graph", "eager"), default="graph",
+                    help="how the end-to-end leg issues a step's launches between its host copies")
     ap.add_argument("--prefetch", type=float, default=None,
                     help="fraction of L2 filled with the next weight by a kernel on a side stream (default: off)")
     ap.add_argument("--next-weight", type=float, default=None,

@@ -181,3 +181,44 @@ def test_group_rejections():
         assert e.value.status == skg.SKG_ERR_ALIGNMENT
     finally:
         g.close()
+
+
+def test_groups_between_other_launches_complete():
+    """The decode-layer chain as launched back to back: five M = 1 GEMV
+    launches, then the M = 8 group, then the M = 64 group, repeated without
+    a host sync.  The groups start while the previous kernels still hold
+    SMs, so only part of a group's grid may be resident at first; every
+    launch must still complete (no bounded wait runs out) and the last run
+    of each group must equal skg_run at the same splits."""
+    def stage_tensors(M, seed):
+        ts = [generate(Projection(M, N, K, epi, seed=seed + i)) for i, (K, N, epi) in enumerate(CHAIN_STAGES)]
+        return ([to_dev(t.x) for t in ts], [to_dev(t.W) for t in ts], [to_dev(t.res) for t in ts],
+                [out_tensor(M, N, epi) for (K, N, epi) in CHAIN_STAGES])
+
+    dims = ([N for _, N, _ in CHAIN_STAGES], [K for K, _, _ in CHAIN_STAGES], [e for _, _, e in CHAIN_STAGES])
+    gemv = stage_tensors(1, 700)
+    plans = [skg.Plan(1, N, K, epi) for (K, N, epi) in CHAIN_STAGES]
+    groups = {M: (skg.Group(M, *dims, [0, 1, 1, 1, 1]), stage_tensors(M, 710 + M)) for M in (8, 64)}
+    try:
+        s = torch.cuda.Stream()
+        for _ in range(300):
+            for i, p in enumerate(plans):
+                p.run(gemv[0][i], gemv[1][i], gemv[2][i], gemv[3][i], s)
+            for M in (8, 64):
+                g, (xs, Ws, rs, ys) = groups[M]
+                g.run(xs, Ws, rs, ys, s)
+        s.synchronize()
+        for p in plans:
+            p.check()
+        for M in (8, 64):
+            g, (xs, Ws, rs, ys) = groups[M]
+            g.check()
+            split = g.info()["split"]
+            for i, (K, N, epi) in enumerate(CHAIN_STAGES):
+                assert np.array_equal(out_bits(ys[i]), _single(M, N, K, epi, split[i], xs[i], Ws[i], rs[i])), \
+                    f"M={M} projection {i} differs from skg_run"
+    finally:
+        for p in plans:
+            p.close()
+        for g, _ in groups.values():
+            g.close()
