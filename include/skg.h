@@ -120,9 +120,12 @@ typedef struct skg_plan_s *skg_plan_t;
 /*
  * skg_plan_query -- the kernel choice and launch shape for (M,N,K,epilogue)
  * on a GPU with num_sms SMs and l2_bytes of L2, without touching any GPU.
- * [TS]: M <= 2 -> SKG_KERNEL_GEMV, M > 2 -> SKG_KERNEL_SPLITK_TC; inside each
- * kind the split and pipeline depth come from a table of measured timings
- * (nearest M for a listed (N,K,epilogue)), else from an occupancy rule.
+ * [TS]: M <= 2 -> SKG_KERNEL_GEMV, M > 2 -> SKG_KERNEL_SPLITK_TC, except that
+ * an M <= 2 shape runs the tensor-core kernel where the table of measured
+ * timings holds a tensor-core row for exactly that (M,N,K,epilogue) (written
+ * only where it beat every GEMV form on GB300); inside each kind the split
+ * and pipeline depth come from that table (nearest M for a listed
+ * (N,K,epilogue)), else from an occupancy rule.
  * Constraints: 1 <= M <= 64, N >= 1, K >= 8 and K % 8 == 0, epilogue valid.
  * Errors: SKG_ERR_INVALID_ARG (sizes, enum, NULL out), SKG_ERR_UNSUPPORTED.
  */
@@ -158,6 +161,19 @@ SKG_API skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out);
  */
 SKG_API skg_status skg_plan_force(skg_plan_t plan, int split_k, int stages, int grid,
                                   int tma_burst);
+
+/*
+ * skg_plan_force_kernel -- run the plan on the given kernel kind
+ * (SKG_KERNEL_GEMV: M <= 2 only; SKG_KERNEL_SPLITK_TC: any M), its launch
+ * shape re-picked as skg_plan_query picks it for that kind; earlier
+ * skg_plan_force overrides are dropped, the PDL setting is kept.  The two
+ * kinds accumulate in different orders, so their results may differ in the
+ * last bits (each within the same error bound).  Workspace as skg_plan_force.
+ * Used by the tuner and the tests.  Errors: SKG_ERR_INVALID_ARG (NULL plan,
+ * unknown kind), SKG_ERR_UNSUPPORTED (GEMV at M > 2, a shape the kind cannot
+ * run), SKG_ERR_CUDA.
+ */
+SKG_API skg_status skg_plan_force_kernel(skg_plan_t plan, int kind);
 
 /*
  * skg_plan_set_pdl -- 1 (default): launch with programmatic dependent launch,

@@ -165,7 +165,17 @@ const TableRow *table_lookup(int kind, int M, int N, int K, int epi)
     return best;
 }
 
-skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg_plan_desc *d)
+bool table_has_exact(int kind, int M, int N, int K, int epi)
+{
+    for (const TableRow *r = kTable; r->kind != 0; ++r)
+        if (r->kind == kind && r->M == M && r->N == N && r->K == K && r->epi == epi)
+            return true;
+    return false;
+}
+
+// force_kind 0: the picker chooses the kernel kind.
+skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg_plan_desc *d,
+                 int force_kind = 0)
 {
     if (!d)
         return fail(SKG_ERR_INVALID_ARG, "skg_plan_query: out is NULL");
@@ -190,8 +200,19 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
     const size_t wbytes = static_cast<size_t>(N) * K * 2;
     d->prefetch_bytes = std::min(wbytes, static_cast<size_t>(0.5 * static_cast<double>(l2_bytes))) & ~static_cast<size_t>(15);
 
-    // [TS]: the kernel kind follows the batch size alone.
-    const int kind = (M <= 2) ? SKG_KERNEL_GEMV : SKG_KERNEL_SPLITK_TC;
+    // [TS]: the kernel kind follows the batch size -- except where the
+    // measured table holds a tensor-core row for exactly this M <= 2 shape
+    // (the tuner writes one only where that kernel beat every GEMV form).
+    int kind = (M <= 2) ? SKG_KERNEL_GEMV : SKG_KERNEL_SPLITK_TC;
+    if (force_kind != 0) {
+        if (force_kind != SKG_KERNEL_GEMV && force_kind != SKG_KERNEL_SPLITK_TC)
+            return fail(SKG_ERR_INVALID_ARG, "unknown kernel kind %d", force_kind);
+        if (force_kind == SKG_KERNEL_GEMV && M > 2)
+            return fail(SKG_ERR_UNSUPPORTED, "the GEMV kernel takes M <= 2 (M=%d)", M);
+        kind = force_kind;
+    } else if (M <= 2 && table_has_exact(SKG_KERNEL_SPLITK_TC, M, N, K, epi)) {
+        kind = SKG_KERNEL_SPLITK_TC;
+    }
     if (kind == SKG_KERNEL_GEMV && gemv_smem_bytes(M, K, 1, 0) > kGemvMaxSmem)
         return fail(SKG_ERR_UNSUPPORTED, "K=%d too large for the M<=2 kernel (x is staged in shared memory)", K);
     const TableRow *row = table_lookup(kind, M, N, K, epi);
@@ -634,6 +655,32 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int t
         fill_tc(&d, split, st, b);
     }
     d.from_table = 0;
+    p->d = d;
+    p->wmaps.clear();
+    p->xmaps.clear();
+    return ensure_workspace(p);
+}
+
+skg_status skg_plan_force_kernel(skg_plan_t p, int kind)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_force_kernel: plan is NULL");
+    skg_plan_desc d;
+    skg_status st = query(p->d.M, p->d.N, p->d.K, p->d.epilogue, p->num_sms, p->l2_bytes, &d, kind);
+    if (st != SKG_OK)
+        return st;
+    d.pdl = p->d.pdl;
+    int ctas = p->gemv_ctas_per_sm;
+    if (d.kernel_kind == SKG_KERNEL_GEMV) {
+        const cudaError_t e = gemv_occupancy(d.M, d.K, d.split_k, d.stages, &ctas);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (ctas < 1)
+            return fail(SKG_ERR_UNSUPPORTED, "the M<=2 kernel cannot be resident with this shape");
+        if (d.split_k > 1 && (!d.from_table || d.grid <= 0))
+            fill_gemv(&d, d.split_k, d.stages, p->num_sms * ctas, p->num_sms);
+    }
+    p->gemv_ctas_per_sm = ctas;
     p->d = d;
     p->wmaps.clear();
     p->xmaps.clear();

@@ -33,7 +33,7 @@ KERNEL_NAMES = {SKG_KERNEL_GEMV: "gemv", SKG_KERNEL_SPLITK_TC: "splitk_tc"}
 
 # Every symbol include/skg.h declares.
 EXPORTS = (
-    "skg_plan_query", "skg_plan", "skg_plan_force", "skg_plan_set_pdl", "skg_run",
+    "skg_plan_query", "skg_plan", "skg_plan_force", "skg_plan_force_kernel", "skg_plan_set_pdl", "skg_run",
     "skg_prefetch_l2", "skg_plan_set_prefetch_fraction", "skg_plan_info", "skg_plan_check",
     "skg_plan_destroy", "skg_debug_wait_timeout", "skg_last_error", "skg_version",
     "skg_run_noalloc", "skg_plan_set_reduction", "skg_plan_set_l2_ahead", "skg_plan_set_next_weight",
@@ -83,6 +83,7 @@ def load(path: str = LIB_PATH):
     lib.skg_plan.argtypes = [i, i, i, i, P(vp)]
     lib.skg_plan_force.argtypes = [vp, i, i, i, i]
     lib.skg_plan_set_pdl.argtypes = [vp, i]
+    lib.skg_plan_force_kernel.argtypes = [vp, i]
     lib.skg_run.argtypes = [vp, vp, vp, vp, vp, vp]
     lib.skg_prefetch_l2.argtypes = [vp, vp, vp]
     lib.skg_plan_set_prefetch_fraction.argtypes = [vp, ctypes.c_double]
@@ -158,6 +159,10 @@ def skg_plan_force(plan: int, split_k: int = 0, stages: int = 0, grid: int = 0, 
     _check(load().skg_plan_force(plan, split_k, stages, grid, tma_burst))
 
 
+def skg_plan_force_kernel(plan: int, kind: int):
+    _check(load().skg_plan_force_kernel(plan, kind))
+
+
 def skg_plan_set_pdl(plan: int, enable: bool):
     _check(load().skg_plan_set_pdl(plan, 1 if enable else 0))
 
@@ -224,6 +229,9 @@ class Plan:
 
     def force(self, split_k: int = 0, stages: int = 0, grid: int = 0, tma_burst: int = 0):
         skg_plan_force(self.handle, split_k, stages, grid, tma_burst)
+
+    def force_kernel(self, kind: int):
+        skg_plan_force_kernel(self.handle, kind)
 
     def set_pdl(self, enable: bool):
         skg_plan_set_pdl(self.handle, enable)

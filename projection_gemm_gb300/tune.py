@@ -17,6 +17,7 @@ import argparse
 import json
 import math
 import os
+import re
 import time
 
 import torch
@@ -50,9 +51,23 @@ def candidates(M, N, K):
         for split in (2, 4, 8):
             for ring in (2, 3, 4):
                 c.append({"split_k": split, "stages": ring, "ahead": 0})
+        # the tensor-core kernel with the tokens padded to 16 columns
+        c += [{"kind": skg.SKG_KERNEL_SPLITK_TC, "split_k": sp, "stages": st, "ahead": a}
+              for sp in (2, 4, 8) for st in (4, 5, 6) for a in (0, 2)]
         return c
     return [{"split_k": s, "stages": st, "ahead": a} for s in (2, 4, 8, 16) for st in (3, 4, 5, 6)
             for a in (0, 2, 4, 6, 8)]
+
+
+def read_rows(path):
+    """The rows of an existing table file, as the tuple main() writes."""
+    rows = []
+    pat = re.compile(r"^\{([-\d, ]+)\},\s*// ([\d.]+) us, ([\d.]+) GB/s")
+    for line in open(path):
+        m = pat.match(line)
+        if m:
+            rows.append(tuple(int(v) for v in m.group(1).split(",")) + (float(m.group(2)), float(m.group(3))))
+    return rows
 
 
 def time_config(M, N, K, epi, cfg, Ws, x, res, y, rounds):
@@ -62,6 +77,8 @@ def time_config(M, N, K, epi, cfg, Ws, x, res, y, rounds):
     p = None
     try:
         p = skg.Plan(M, N, K, epi)
+        if cfg.get("kind"):
+            p.force_kernel(cfg["kind"])
         force = {k: v for k, v in cfg.items() if k in ("split_k", "stages", "tma_burst") and v}
         p.force(**force)
         p.set_l2_ahead(cfg.get("ahead", 0))
@@ -100,7 +117,14 @@ def main(argv=None):
     ap.add_argument("--out-inc", default=INC)
     ap.add_argument("--out-log", default=None)
     ap.add_argument("--rounds", type=int, default=40)
+    ap.add_argument("--only-m", type=int, nargs="*", default=None,
+                    help="tune only these M; the table's rows (and the log's entries) for other M are kept")
     args = ap.parse_args(argv)
+    kept_rows, kept_log = [], []
+    if args.only_m:
+        kept_rows = [r for r in read_rows(args.out_inc) if r[1] not in args.only_m]
+        if args.out_log and os.path.exists(args.out_log):
+            kept_log = [e for e in json.load(open(args.out_log)) if e["M"] not in args.only_m]
     build.build()
     skg.load()
     torch.cuda.set_device(0)
@@ -114,6 +138,8 @@ def main(argv=None):
         Ws = [base.roll(i, dims=0).contiguous() for i in range(copies)]   # distinct bytes, same statistics
         del base
         for M in ms:
+            if args.only_m and M not in args.only_m:
+                continue
             t = generate(Projection(M, N, K, epi, seed=901 + M))
             x = t.x.cuda()
             res = None if t.res is None else t.res.cuda()
@@ -135,6 +161,8 @@ def main(argv=None):
             print(f"N={N} K={K} {epi} M={M}: best {cfg} {us:.2f} us {wbytes / us / 1e3:.0f} GB/s", flush=True)
         del Ws
         torch.cuda.empty_cache()
+    rows = sorted(kept_rows + rows, key=lambda r: (r[2], r[3], r[4], r[1]))
+    log = kept_log + log
     with open(args.out_inc, "w") as f:
         f.write("// skg_plan_table.inc -- measured picker table.\n//\n"
                 "// Each row: { kernel_kind, M, N, K, epilogue, split_k, stages, grid, tma_burst, l2_ahead }.\n"

@@ -6,6 +6,7 @@ import re
 import pytest
 
 from projection_gemm_gb300 import build, skg
+from tests.plan_table import expected_kind
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "skg.h")
@@ -44,10 +45,10 @@ def test_library_is_sm103a_only():
 @pytest.mark.parametrize("M", range(1, 65))
 def test_kernel_kind_follows_batch(M):
     d = skg.skg_plan_query(M, 7168, 7168, "bf16", SMS, L2)
-    assert d["kernel"] == ("gemv" if M <= 2 else "splitk_tc")
+    assert d["kernel"] == expected_kind(M, 7168, 7168, "bf16")
     s = d["split_k"]
     assert s & (s - 1) == 0 and 16 % s == 0
-    if M > 2:
+    if d["kernel"] == "splitk_tc":
         assert s >= 2
         assert d["m_pad"] == (M + 15) // 16 * 16
         assert d["grid"] == 56 * s

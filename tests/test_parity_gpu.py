@@ -19,6 +19,7 @@ from projection_gemm_gb300.inputs import (CHAIN_M, DEEPK_M, SWEEP_M, WIDE_M, Pro
                                           chain, deepk, generate, pr1, sweep, wide)
 from tests import tolerance as T
 from tests.gpu_util import DeviceCase, out_bits, out_tensor
+from tests.plan_table import expected_kind
 
 pytestmark = pytest.mark.gpu
 
@@ -82,7 +83,7 @@ def test_small_shapes_all_splits(M, N, K, epi):
     case = DeviceCase(p)
     try:
         info = case.plan.info()
-        assert info["kernel"] == ("gemv" if M <= 2 else "splitk_tc")
+        assert info["kernel"] == expected_kind(M, N, K, epi)
         base = case.run_bits()
         full_check(case, base, what=f"{p} default split {info['split_k']}")
         ran = force_each_split(case, base, M)
@@ -107,6 +108,8 @@ def test_gemv_row_forms_bit_identical(M, N, K, epi):
     p = Projection(M, N, K, epi, seed=2000 + M + N + K, residual_var=1.0)
     case = DeviceCase(p)
     try:
+        if case.plan.info()["kernel"] != "gemv":      # the table gave this shape to the tensor-core kernel
+            case.plan.force_kernel(skg.SKG_KERNEL_GEMV)
         base = case.run_bits()
         if M * N * K <= 2 * 4096 * 4104:
             full_check(case, base, what=f"{p} default")
@@ -134,6 +137,39 @@ def test_gemv_row_forms_bit_identical(M, N, K, epi):
             assert np.array_equal(got, base), f"stages {stages} grid {grid} changed the bits of {p}"
             ran.append((stages, grid, batch))
         assert len(ran) >= (10 if K % 256 == 0 else 2), ran
+        case.plan.check()
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("M,N,K,epi", [(1, 1000, 1048, "bf16"), (2, 129, 72, "bf16_residual"),
+                                       (1, 384, 7168, "fp32"), (2, 7168, 7168, "bf16")], ids=lambda v: str(v))
+def test_tensor_core_kernel_at_m_le_2(M, N, K, epi):
+    """skg_plan_force_kernel puts an M <= 2 plan on the tensor-core kernel
+    (tokens padded to 16 columns): it meets the oracle, and every split
+    gives the same bits; back on the GEMV it meets the oracle too."""
+    p = Projection(M, N, K, epi, seed=2100 + M + N + K, residual_var=1.0)
+    case = DeviceCase(p)
+    try:
+        case.plan.force_kernel(skg.SKG_KERNEL_SPLITK_TC)
+        info = case.plan.info()
+        assert info["kernel"] == "splitk_tc" and info["m_pad"] == 16
+        base = case.run_bits()
+        if M * N * K <= 2 * 4096 * 4104:
+            full_check(case, base, what=f"{p} tensor-core kernel")
+        else:
+            xb, wb, rb = case.host_bits()
+            rng = np.random.default_rng(p.seed)
+            ns, ms = rng.integers(0, N, 3000), rng.integers(0, M, 3000)
+            y_ref, s1 = O.linear_points(xb, wb, ms, ns, rb)
+            T.check(base[ms, ns], y_ref, s1, K, fp32=epi == "fp32", what=f"{p} tensor-core kernel sampled")
+        for split in (2, 4, 8, 16):
+            case.plan.force(split_k=split)
+            assert np.array_equal(case.run_bits(), base), f"split {split} changed the bits of {p}"
+        case.plan.force_kernel(skg.SKG_KERNEL_GEMV)
+        assert case.plan.info()["kernel"] == "gemv"
+        if M * N * K <= 2 * 4096 * 4104:
+            full_check(case, case.run_bits(), what=f"{p} back on the GEMV")
         case.plan.check()
     finally:
         case.close()
@@ -217,7 +253,7 @@ def _sampled_check(p: Projection, npts=3000, extra_rows=()):
 @pytest.mark.parametrize("M", SWEEP_M)
 def test_sweep_full_size_sampled(M):
     ratio, info = _sampled_check(sweep(M))
-    assert info["kernel"] == ("gemv" if M <= 2 else "splitk_tc")
+    assert info["kernel"] == expected_kind(M, 7168, 7168, "bf16")
 
 
 @pytest.mark.parametrize("M", WIDE_M)
