@@ -3,9 +3,13 @@ for profilers (ncu captures of a single kernel launch).
 
 usage: python -m projection_gemm_gb300.profile_case M N K [epilogue] [launches]
                                                     [--split S] [--stages D]
+       python -m projection_gemm_gb300.profile_case M --chain-group [launches]
 The operands are the seeded synthetic tensors of `inputs.py` (seed 11); the
 default plan is used unless --split / --stages force a configuration (as
-skg_plan_force does); the process exits non-zero on any library error.
+skg_plan_force does).  --chain-group runs the five decode-layer chain
+projections at M as one group launch (skg_group, each projection ordered
+after the previous one) instead.  The process exits non-zero on any library
+error.
 """
 import argparse
 import sys
@@ -16,7 +20,33 @@ from . import build, skg
 from .inputs import Projection, generate
 
 
+def chain_group(M, launches):
+    from .inputs import CHAIN_STAGES
+    ts = [generate(Projection(M, N, K, epi, seed=11 + i)) for i, (K, N, epi) in enumerate(CHAIN_STAGES)]
+    xs = [t.x.cuda() for t in ts]
+    Ws = [t.W.cuda() for t in ts]
+    rs = [None if t.res is None else t.res.cuda() for t in ts]
+    ys = [torch.empty(M, N, dtype=torch.float32 if epi == "fp32" else torch.bfloat16, device="cuda")
+          for (K, N, epi) in CHAIN_STAGES]
+    g = skg.Group(M, [N for _, N, _ in CHAIN_STAGES], [K for K, _, _ in CHAIN_STAGES],
+                  [e for _, _, e in CHAIN_STAGES], [0, 1, 1, 1, 1])
+    print(g.info())
+    for _ in range(launches):
+        g.run(xs, Ws, rs, ys)
+    torch.cuda.synchronize()
+    g.check()
+    g.close()
+    print("ok")
+
+
 def main(argv):
+    if "--chain-group" in argv:
+        rest = [a for a in argv if a != "--chain-group"]
+        build.build()
+        skg.load()
+        torch.cuda.set_device(0)
+        chain_group(int(rest[0]), int(rest[1]) if len(rest) > 1 else 3)
+        return
     ap = argparse.ArgumentParser()
     ap.add_argument("M", type=int)
     ap.add_argument("N", type=int)
