@@ -252,11 +252,11 @@ class GroupProjection:
         return sum(p.flops() for p in self.members)
 
 
-def make_group(members):
+def make_group(members, ordered=True):
     from projection_gemm_gb300 import skg
     ps = [o["p"] for o in members]
     g = skg.Group(ps[0].M, [p.N for p in ps], [p.K for p in ps], [p.epilogue for p in ps],
-                  [0] + [1] * (len(ps) - 1))
+                  [0] + [1 if ordered else 0] * (len(ps) - 1))
     info = g.info()
     return dict(p=GroupProjection(ps), group=g, plans=[o["plan"] for o in members],
                 info={"kernel": "splitk_group", "split_k": info["split"], "prefetch_bytes": 0,
@@ -346,7 +346,8 @@ def run_ours(args):
 
     # --fused: each run of consecutive projections with the same M >= 3 is
     # one group launch (skg_group), every projection after the first ordered
-    # after the previous one (dep), as consecutive launches are.
+    # after the previous one (dep), as consecutive launches are -- or, with
+    # --fused-order independent, with no order among them.
     if args.fused:
         side_pf = False
         segs, i = [], 0
@@ -354,7 +355,7 @@ def run_ours(args):
             j = i + 1
             while ops[i]["p"].M >= 3 and j < len(ops) and ops[j]["p"].M == ops[i]["p"].M:
                 j += 1
-            segs.append(ops[i] if j == i + 1 else make_group(ops[i:j]))
+            segs.append(ops[i] if j == i + 1 else make_group(ops[i:j], args.fused_order == "chain"))
             i = j
         ops = segs
 
@@ -501,6 +502,9 @@ def run_ours(args):
                    "l2": ("inputs larger than L2: every step streams %.1f MB of distinct weights" % (wbytes_step / 1e6)),
                    "pdl": bool(args.pdl),
                    "fused_groups": bool(args.fused),
+                   **({"fused_order": ("each projection of a group after the previous one" if args.fused_order == "chain"
+                                       else "the projections of a group independent of one another")}
+                      if args.fused else {}),
                    "launch": ("cuda graph of the step's launches, replayed (steps carrying events run eagerly)"
                               if args.graph else "eager skg_run calls"),
                    "next_weight_l2_fraction": next_frac,
@@ -611,6 +615,9 @@ def main(argv=None):
                          "(default: 0.15 for the chain, off otherwise)")
     ap.add_argument("--fused", type=int, default=0,
                     help="1: consecutive projections of one M >= 3 as one group launch (skg_group)")
+    ap.add_argument("--fused-order", choices=("chain", "independent"), default="chain",
+                    help="with --fused: order each projection after the previous one (as consecutive launches "
+                         "are), or run a group's projections as independent work (e.g. projections of one x)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
