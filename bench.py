@@ -355,7 +355,8 @@ def run_ours(args):
             j = i + 1
             while ops[i]["p"].M >= 3 and j < len(ops) and ops[j]["p"].M == ops[i]["p"].M:
                 j += 1
-            segs.append(ops[i] if j == i + 1 else make_group(ops[i:j], args.fused_order == "chain"))
+            single = j == i + 1 and not (args.fused_single and ops[i]["p"].M >= 3)
+            segs.append(ops[i] if single else make_group(ops[i:j], args.fused_order == "chain"))
             i = j
         ops = segs
 
@@ -618,6 +619,9 @@ def main(argv=None):
     ap.add_argument("--fused-order", choices=("chain", "independent"), default="chain",
                     help="with --fused: order each projection after the previous one (as consecutive launches "
                          "are), or run a group's projections as independent work (e.g. projections of one x)")
+    ap.add_argument("--fused-single", type=int, default=0,
+                    help="with --fused: a projection of M >= 3 with no same-M neighbour also runs as a "
+                         "one-projection group (units handed out dynamically)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
