@@ -1062,6 +1062,10 @@ skg_status skg_group_run(skg_group_t g, const void *const *x, const void *const 
         P.unit_begin = unit;
         unit += g->n_tiles[i] * g->split[i];
     }
+    gp.static_first = 1;
+    for (int i = 1; i < g->n; ++i)
+        if (g->dep[i])
+            gp.static_first = 0;
     gp.done = reinterpret_cast<unsigned int *>(base + g->done_off);
     gp.err = g->err_dev;
     gp.n = g->n;

@@ -198,13 +198,25 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
             auto slot_free = [&](int k) {
                 return k < S || mbar_wait(&empty[k % S], ((k / S) & 1) ^ 1, g.timeout_ns, &flags[0]);
             };
-            // Until the previous grid completes, warm L2 with the first
-            // weight tiles of unit blockIdx.x: the first units handed out
-            // are 0 .. grid - 1, in whatever order the CTAs arrive.
+            // Until the previous grid completes: with no dependencies in the
+            // group nothing ever waits for another CTA's unit, so CTA c owns
+            // unit c outright and fills its ring with that unit's weights (as
+            // the one-projection kernel does); otherwise every unit comes from
+            // the counter, and the CTA only warms L2 with the first tiles of
+            // unit c (units 0 .. grid - 1 go out first, in whatever order the
+            // CTAs arrive).
+            const bool own_first = g.static_first != 0;
+            int armed0 = 0;
             if (static_cast<int>(blockIdx.x) < g.units) {
                 const Unit U0 = unit_of(g, blockIdx.x);
                 const GroupProj &P0 = g.proj[U0.j];
-                for (int i = 0; i < U0.nk && i < S + P0.ahead; ++i)
+                const int pre0 = own_first ? (U0.nk < S ? U0.nk : S) : 0;
+                for (; armed0 < pre0; ++armed0) {       // every slot is free at the start
+                    mbar_arrive_expect_tx(&full[armed0], kWBytes + Sh::kXBytes);
+                    tma_load_2d(sW + armed0 * kWBytes, &P0.tmW, &full[armed0], (U0.kb_begin + armed0) * kBlockK,
+                                U0.tile * kTileN, pol_w);
+                }
+                for (int i = pre0; i < U0.nk && i < pre0 + (own_first ? P0.ahead : S + P0.ahead); ++i)
                     tma_prefetch_l2_2d(&P0.tmW, (U0.kb_begin + i) * kBlockK, U0.tile * kTileN);
             }
             pdl_wait();   // the unit counter and x only from here on
@@ -214,7 +226,9 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
                     ok = false;
                     break;
                 }
-                const unsigned u = atomicAdd(&g.done[kGroupDoneNext], 1u);
+                const unsigned u = (own_first && q == 0)
+                                       ? blockIdx.x
+                                       : (own_first ? gridDim.x : 0u) + atomicAdd(&g.done[kGroupDoneNext], 1u);
                 const bool last = u >= static_cast<unsigned>(g.units);
                 uq[q % Q] = last ? -1 : static_cast<int>(u);
                 mbar_arrive(&uq_full[q % Q]);
@@ -227,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
                 const int tile_row = U.tile * kTileN;
                 const int pre = U.nk < S ? U.nk : S;
                 // the first weight tiles need no wait (weights are static)
-                int armed = 0;
+                int armed = (own_first && q == 0) ? armed0 : 0;
                 for (; armed < pre; ++armed) {
                     if (!slot_free(it + armed))
                         break;

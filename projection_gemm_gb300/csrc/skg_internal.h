@@ -106,6 +106,7 @@ struct GroupParams {
                             // finished, [kGroupDoneNext] units handed out
     unsigned int *err;
     int n, M, units, stages;
+    int static_first;       // 1 (no dependencies): CTA c's first unit is unit c, the counter hands out the rest
     unsigned long long timeout_ns;
 };
 
