@@ -2,11 +2,11 @@
 for profilers (ncu captures of a single kernel launch).
 
 usage: python -m projection_gemm_gb300.profile_case M N K [epilogue] [launches]
-                                                    [--split S] [--stages D]
+                                                    [--kind gemv|tc] [--split S] [--stages D] [--burst B]
        python -m projection_gemm_gb300.profile_case M --chain-group [launches]
 The operands are the seeded synthetic tensors of `inputs.py` (seed 11); the
-default plan is used unless --split / --stages force a configuration (as
-skg_plan_force does).  --chain-group runs the five decode-layer chain
+default plan is used unless --kind (skg_plan_force_kernel) or --split /
+--stages / --burst (skg_plan_force) force a configuration.  --chain-group runs the five decode-layer chain
 projections at M as one group launch (skg_group, each projection ordered
 after the previous one) instead.  The process exits non-zero on any library
 error.
@@ -53,8 +53,10 @@ def main(argv):
     ap.add_argument("K", type=int)
     ap.add_argument("epilogue", nargs="?", default="bf16")
     ap.add_argument("launches", nargs="?", type=int, default=3)
+    ap.add_argument("--kind", choices=("gemv", "tc"), default=None)
     ap.add_argument("--split", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--burst", type=int, default=0)
     a = ap.parse_args(argv)
     M, N, K, epi, launches = a.M, a.N, a.K, a.epilogue, a.launches
     build.build()
@@ -65,8 +67,10 @@ def main(argv):
     res = None if t.res is None else t.res.cuda()
     y = torch.empty(M, N, dtype=torch.float32 if epi == "fp32" else torch.bfloat16, device="cuda")
     plan = skg.Plan(M, N, K, epi)
-    if a.split or a.stages:
-        plan.force(split_k=a.split, stages=a.stages)
+    if a.kind:
+        plan.force_kernel(skg.SKG_KERNEL_GEMV if a.kind == "gemv" else skg.SKG_KERNEL_SPLITK_TC)
+    if a.split or a.stages or a.burst:
+        plan.force(split_k=a.split, stages=a.stages, tma_burst=a.burst)
     print(plan.info())
     for _ in range(launches):
         plan.run(x, W, res, y)
