@@ -316,3 +316,26 @@ def test_rejections_launch_nothing():
             skg.Plan(*bad, "bf16")
     with pytest.raises(skg.SkgError):
         skg.Plan(4, 128, 128, 7)
+
+
+def test_force_kernel_rejections_keep_the_plan():
+    """The GEMV takes M <= 2 only; an unknown kind is an argument error; a
+    rejected request leaves the plan as it was, still runnable."""
+    p = Projection(4, 300, 1048, "bf16", seed=2200)
+    case = DeviceCase(p)
+    try:
+        before = case.plan.info()
+        base = case.run_bits()
+        with pytest.raises(skg.SkgError) as e:
+            case.plan.force_kernel(skg.SKG_KERNEL_GEMV)
+        assert e.value.status == skg.SKG_ERR_UNSUPPORTED
+        with pytest.raises(skg.SkgError) as e:
+            case.plan.force_kernel(7)
+        assert e.value.status == skg.SKG_ERR_INVALID_ARG
+        assert case.plan.info() == before
+        assert np.array_equal(case.run_bits(), base)
+        case.plan.force_kernel(skg.SKG_KERNEL_SPLITK_TC)      # the kind it already has: same bits
+        assert np.array_equal(case.run_bits(), base)
+        case.plan.check()
+    finally:
+        case.close()
