@@ -354,7 +354,7 @@ def run_ours(args):
             nxt = ops[(i + 1) % len(ops)]
             o["plan"].set_next_weight(nxt["W"], int(min(nxt["p"].weight_bytes(), next_frac * l2)))
 
-    # --fused: each run of consecutive projections with the same M >= 3 is
+    # --fused: each run of consecutive projections with the same M >= --fused-min-m is
     # one group launch (skg_group), every projection after the first ordered
     # after the previous one (dep), as consecutive launches are -- or, with
     # --fused-order independent, with no order among them.
@@ -363,9 +363,9 @@ def run_ours(args):
         segs, i = [], 0
         while i < len(ops):
             j = i + 1
-            while ops[i]["p"].M >= 3 and j < len(ops) and ops[j]["p"].M == ops[i]["p"].M:
+            while ops[i]["p"].M >= args.fused_min_m and j < len(ops) and ops[j]["p"].M == ops[i]["p"].M:
                 j += 1
-            single = j == i + 1 and not (args.fused_single and ops[i]["p"].M >= 3)
+            single = j == i + 1 and not (args.fused_single and ops[i]["p"].M >= args.fused_min_m)
             segs.append(ops[i] if single else make_group(ops[i:j], args.fused_order == "chain"))
             i = j
         ops = segs
@@ -514,7 +514,8 @@ def run_ours(args):
                    "pdl": bool(args.pdl),
                    "fused_groups": bool(args.fused),
                    **({"fused_order": ("each projection of a group after the previous one" if args.fused_order == "chain"
-                                       else "the projections of a group independent of one another")}
+                                       else "the projections of a group independent of one another"),
+                       "fused_min_m": args.fused_min_m}
                       if args.fused else {}),
                    "launch": ("cuda graph of the step's launches, replayed (steps carrying events run eagerly)"
                               if args.graph else "eager skg_run calls"),
@@ -626,12 +627,15 @@ def main(argv=None):
                     help="fraction of L2 of the next projection's weight each launch asks the L2 for "
                          "(default: 0.15 for the chain, off otherwise)")
     ap.add_argument("--fused", type=int, default=0,
-                    help="1: consecutive projections of one M >= 3 as one group launch (skg_group)")
+                    help="1: consecutive projections of one M (>= --fused-min-m) as one group launch (skg_group)")
     ap.add_argument("--fused-order", choices=("chain", "independent"), default="chain",
                     help="with --fused: order each projection after the previous one (as consecutive launches "
                          "are), or run a group's projections as independent work (e.g. projections of one x)")
+    ap.add_argument("--fused-min-m", type=int, default=3,
+                    help="with --fused: the smallest M whose projections are grouped (M <= 2 groups run the "
+                         "split-K kernel, in place of the GEMV)")
     ap.add_argument("--fused-single", type=int, default=0,
-                    help="with --fused: a projection of M >= 3 with no same-M neighbour also runs as a "
+                    help="with --fused: a projection with no same-M neighbour also runs as a "
                          "one-projection group (units handed out dynamically)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")

@@ -308,7 +308,7 @@ SKG_API const char *skg_last_error(void);
 SKG_API int skg_version(void);
 
 /*
- * Groups -- several projections of the same M (3..64) in one persistent
+ * Groups -- several projections of the same M (1..64) in one persistent
  * split-K launch.  [OC] fuses producer and consumer in one kernel across
  * GPUs; this is the one-GPU form of that idea: the launch's CTAs take the
  * work units (projection, 128-row tile, split) from a counter in projection
@@ -316,8 +316,10 @@ SKG_API int skg_version(void);
  * their TMA ring, TMEM and barriers from one unit to the next, and stream
  * the next projection's weights while the previous one is still being
  * reduced, so consecutive projections pay no launch head or tail between
- * them.  Each projection's output has the bits of skg_run at the same split
- * (splits above 8 are lowered to 8: any split gives the same bits).
+ * them.  Each projection's output has the bits of skg_run on the split-K
+ * kernel at the same split (splits above 8 are lowered to 8: any split gives
+ * the same bits; at M <= 2 that is the plan after
+ * skg_plan_force_kernel(SKG_KERNEL_SPLITK_TC)).
  *
  * skg_group -- plan n (1..8) projections: N[i], K[i] and epilogue[i] as for
  * skg_plan; dep[i] (i >= 1; dep may be NULL for none) = 1: projection i

@@ -909,8 +909,8 @@ skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilog
         return fail(SKG_ERR_UNSUPPORTED, "skg_group: n=%d outside 1..%d", n, kGroupMax);
     if (!N || !K || !epilogue)
         return fail(SKG_ERR_INVALID_ARG, "skg_group: N, K and epilogue must be non-NULL");
-    if (M < 3 || M > 64)
-        return fail(SKG_ERR_UNSUPPORTED, "skg_group: M=%d; groups run the split-K kernel (M = 3..64)", M);
+    if (M < 1 || M > 64)
+        return fail(SKG_ERR_UNSUPPORTED, "skg_group: M=%d outside 1..64", M);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -936,7 +936,9 @@ skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilog
     size_t off = 0;
     for (int i = 0; i < n; ++i) {
         skg_plan_desc d;
-        const skg_status st = query(M, N[i], K[i], epilogue[i], sms, static_cast<size_t>(l2), &d);
+        // the split-K kernel's launch shape for this projection (at M <= 2 too)
+        const skg_status st =
+            query(M, N[i], K[i], epilogue[i], sms, static_cast<size_t>(l2), &d, SKG_KERNEL_SPLITK_TC);
         if (st != SKG_OK) {
             delete g;
             return st;

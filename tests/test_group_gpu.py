@@ -33,6 +33,7 @@ def _lib():
 def _single(M, N, K, epi, split, x, W, res):
     p = skg.Plan(M, N, K, epi)
     try:
+        p.force_kernel(skg.SKG_KERNEL_SPLITK_TC)       # groups run the split-K kernel at every M
         p.force(split_k=split)
         y = out_tensor(M, N, epi)
         p.run(x, W, res, y)
@@ -83,6 +84,8 @@ def test_decode_layer_group_matches_skg_run(M):
 
 
 @pytest.mark.parametrize("M,shapes", [
+    (1, [(1048, 1000, "bf16"), (72, 129, "bf16_residual"), (7168, 384, "fp32")]),
+    (2, [(4096, 7168, "bf16_residual"), (7168, 4096, "bf16")]),
     (3, [(1048, 1000, "bf16"), (72, 129, "bf16_residual"), (2056, 640, "fp32")]),
     (17, [(200, 300, "bf16"), (1024, 1024, "bf16_residual")]),
     (64, [(8, 128, "bf16"), (7168, 384, "fp32"), (520, 4096, "bf16_residual"), (1048, 1, "bf16")]),
@@ -92,7 +95,7 @@ def test_ragged_groups_without_dependencies(M, shapes):
     _group_case(M, shapes, dep=None, seed=400 + M, runs=2)
 
 
-@pytest.mark.parametrize("M", (5, 16, 64))
+@pytest.mark.parametrize("M", (1, 5, 16, 64))
 def test_dependent_chain_reads_the_previous_output(M):
     """x of projection 1 is y of projection 0 (dep set), y0 poisoned before every run."""
     t0 = generate(Projection(M, 4096, 7168, "bf16", seed=500 + M))
@@ -113,6 +116,7 @@ def test_dependent_chain_reads_the_previous_output(M):
         for i, (N, K, epi, x, W, r) in enumerate(chain):
             p = skg.Plan(M, N, K, epi)
             try:
+                p.force_kernel(skg.SKG_KERNEL_SPLITK_TC)
                 p.force(split_k=split[i])
                 p.run(x, W, r, ref_y[i])
                 torch.cuda.synchronize()
@@ -161,7 +165,7 @@ def test_group_captures_into_a_cuda_graph():
 
 def test_group_rejections():
     with pytest.raises(skg.SkgError) as e:
-        skg.Group(2, [128], [128], ["bf16"])
+        skg.Group(65, [128], [128], ["bf16"])
     assert e.value.status == skg.SKG_ERR_UNSUPPORTED
     with pytest.raises(skg.SkgError) as e:
         skg.Group(8, [128] * 9, [128] * 9, ["bf16"] * 9)
