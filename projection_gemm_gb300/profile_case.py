@@ -3,13 +3,13 @@ for profilers (ncu captures of a single kernel launch).
 
 usage: python -m projection_gemm_gb300.profile_case M N K [epilogue] [launches]
                                                     [--kind gemv|tc] [--split S] [--stages D] [--burst B]
-       python -m projection_gemm_gb300.profile_case M --chain-group [launches]
+       python -m projection_gemm_gb300.profile_case M --chain-group [--independent] [launches]
 The operands are the seeded synthetic tensors of `inputs.py` (seed 11); the
 default plan is used unless --kind (skg_plan_force_kernel) or --split /
 --stages / --burst (skg_plan_force) force a configuration.  --chain-group runs the five decode-layer chain
 projections at M as one group launch (skg_group, each projection ordered
-after the previous one) instead.  The process exits non-zero on any library
-error.
+after the previous one, or with --independent in no order) instead.  The
+process exits non-zero on any library error.
 """
 import argparse
 import sys
@@ -20,7 +20,7 @@ from . import build, skg
 from .inputs import Projection, generate
 
 
-def chain_group(M, launches):
+def chain_group(M, launches, ordered=True):
     from .inputs import CHAIN_STAGES
     ts = [generate(Projection(M, N, K, epi, seed=11 + i)) for i, (K, N, epi) in enumerate(CHAIN_STAGES)]
     xs = [t.x.cuda() for t in ts]
@@ -29,7 +29,7 @@ def chain_group(M, launches):
     ys = [torch.empty(M, N, dtype=torch.float32 if epi == "fp32" else torch.bfloat16, device="cuda")
           for (K, N, epi) in CHAIN_STAGES]
     g = skg.Group(M, [N for _, N, _ in CHAIN_STAGES], [K for K, _, _ in CHAIN_STAGES],
-                  [e for _, _, e in CHAIN_STAGES], [0, 1, 1, 1, 1])
+                  [e for _, _, e in CHAIN_STAGES], [0, 1, 1, 1, 1] if ordered else None)
     print(g.info())
     for _ in range(launches):
         g.run(xs, Ws, rs, ys)
@@ -41,11 +41,11 @@ def chain_group(M, launches):
 
 def main(argv):
     if "--chain-group" in argv:
-        rest = [a for a in argv if a != "--chain-group"]
+        rest = [a for a in argv if a not in ("--chain-group", "--independent")]
         build.build()
         skg.load()
         torch.cuda.set_device(0)
-        chain_group(int(rest[0]), int(rest[1]) if len(rest) > 1 else 3)
+        chain_group(int(rest[0]), int(rest[1]) if len(rest) > 1 else 3, "--independent" not in argv)
         return
     ap = argparse.ArgumentParser()
     ap.add_argument("M", type=int)
