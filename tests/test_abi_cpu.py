@@ -121,3 +121,27 @@ def test_one_wave_grid_keeps_rows_per_cta_bounded():
     # a very tall weight: at most 256 rows per CTA, so the grid grows past one wave
     d = skg.skg_plan_query(1, 300000, 1024, "bf16", SMS, L2)
     assert d["stages"] == 3 and -(-300000 // d["grid"]) <= 256
+
+
+def test_plan_table_rows_are_well_formed():
+    """The measured table (rewritten by tune.py, partly with --only-m): one row
+    per (M, N, K, epilogue), valid kinds and launch fields, and every row's
+    shape picks that row's kernel kind."""
+    from projection_gemm_gb300 import tune
+    rows = tune.read_rows(tune.INC)
+    assert rows
+    keys = [(r[1], r[2], r[3], r[4]) for r in rows]
+    assert len(keys) == len(set(keys))
+    for kind, M, N, K, epi, split, stages, grid, burst, ahead, us, gbs in rows:
+        assert kind in (skg.SKG_KERNEL_GEMV, skg.SKG_KERNEL_SPLITK_TC)
+        assert 1 <= M <= 64 and N >= 1 and K % 8 == 0 and epi in (0, 1, 2)
+        assert split & (split - 1) == 0 and 16 % split == 0
+        if kind == skg.SKG_KERNEL_GEMV:
+            assert M <= 2 and split <= 8
+        else:
+            assert split >= 2 and 2 <= stages <= 16 and burst >= 1 and 0 <= ahead <= 16
+        assert us > 0 and 0 < gbs < 8000          # no launch streams faster than the HBM
+        epi_name = {0: "bf16", 1: "bf16_residual", 2: "fp32"}[epi]
+        d = skg.skg_plan_query(M, N, K, epi_name, SMS, L2)
+        assert d["kernel"] == ("gemv" if kind == skg.SKG_KERNEL_GEMV else "splitk_tc")
+        assert d["split_k"] == split and d["from_table"] == 1
