@@ -10,17 +10,37 @@ one batch of synthetic inputs:
                    102.8 MB weight (seed = index of M), so a step streams
                    719 MB of weights and no weight is L2-resident when its
                    projection runs (inputs larger than the 126 MB L2).
-  chain            the five projections of a decode layer at M = 1, 8, 64,
-                   each launch asking the L2 for the start of the next weight.
+  chain            the five projections of a decode layer at M = 1, 8, 64.
   wide / deepk     the wide input projection and the deep-K output projection
                    with residual, at their M values.
+  pr1              the single M = 1, K = N = 1024 projection with residual.
 
-`value` is the whole job's weight bytes / device time (CUDA events around the
-timed steps, max over ranks).  `e2e` repeats the measurement through the
-public API with the step's activations copied from pinned host memory and its
-outputs copied back inside the timed region (weights stay resident: they are
-parameters, not per-step inputs).  `--impl reference` times the CPU oracle on
-the same metric instead (a bounded sample of each step).
+The headline `value` is the whole job's weight bytes / device time of exactly
+`--steps` eager steps (CUDA events only at the two ends of the timed region,
+max over ranks).  Every other figure comes from separate passes after it, so
+no event sits between two launches of the timed region (an event between two
+launches ends their programmatic overlap):
+
+  per_projection   for every projection of the step, `us_back_to_back`: a run
+                   of launches of that projection alone, each over a different
+                   copy of its weight (the copies together exceed twice the
+                   L2), events at the two ends of the run, time / launches;
+                   `us_event_isolated`: events before and after each launch in
+                   sampled steps.
+  roofline         the dominant kernel (most device time in the step): its
+                   projections' algorithmic bytes summed / their
+                   back-to-back times summed, against the measured HBM peak.
+  kernel_in_step   each kernel kind's consecutive launches inside sampled
+                   steps, events at the kind boundaries only.
+  configs          the other named workloads (wide, deep-K, PR1, the chain
+                   with and without the L2 prefetch of the next weight) with
+                   the same fields, unless --headline-only.
+
+`e2e` repeats the headline measurement through the public API with the
+step's activations copied from pinned host memory and its outputs copied
+back inside the timed region (weights stay resident: they are parameters,
+not per-step inputs).  `--impl reference` times the CPU oracle on the same
+metric instead (a bounded sample of each step).
 """
 from __future__ import annotations
 
@@ -40,6 +60,7 @@ sys.path.insert(0, ROOT)
 METRIC = "weight-stream GB/s and µs/projection vs GB300 HBM roofline at M=1..64"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+EXTRA_CONFIGS = ("wide", "deepk", "pr1", "chain")
 
 
 # ------------------------------------------------------------------ workloads
@@ -60,8 +81,8 @@ def workload(name: str):
     if name == "chain":
         projs = [p for m in I.CHAIN_M for p in I.chain(m)]
         return projs, ("decode-layer chain at M in {1,8,64}: 7168->12288, 8192->7168 (+res), "
-                       "7168->384 (fp32), 7168->4096, 4096->7168 (+res); each launch asks the L2 "
-                       "for the start of the next W"), {"M": list(I.CHAIN_M), "stages": [list(s) for s in I.CHAIN_STAGES]}
+                       "7168->384 (fp32), 7168->4096, 4096->7168 (+res)"), \
+            {"M": list(I.CHAIN_M), "stages": [list(s) for s in I.CHAIN_STAGES]}
     if name == "pr1":
         return [I.pr1()], "PR1: M=1, K=N=1024, + residual", {"M": [1], "N": 1024, "K": 1024,
                                                               "epilogue": "bf16_residual"}
@@ -107,22 +128,22 @@ def kernel_traffic(kernel: str, workload: str):
 
 # --------------------------------------------------------------- clock probe
 class ClockSampler:
-    """nvidia-smi samples (200 ms) while the timed region runs."""
+    """nvidia-smi samples (every 100 ms) while the GPU passes run."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: str):
         self.samples = []
         self.proc = None
         self.gpu = gpu_index
-        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -133,9 +154,6 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.samples.append((time.time(), line.strip()))
 
-    def window(self, t0, t1):
-        self.t0, self.t1 = t0, t1
-
     def stop(self):
         if self.proc:
             self.proc.terminate()
@@ -144,12 +162,11 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
-        rows = [s for t, s in self.samples if self.t0 is not None and self.t0 - 0.1 <= t <= self.t1 + 0.25]
-        if not rows and self.samples:
-            rows = [self.samples[-1][1]]
+    def summary(self, windows):
+        """Median SM clock and the reasons seen over the given (t0, t1)
+        windows (each widened by one sampling period)."""
+        rows = [s for t, s in self.samples if any(a - 0.1 <= t <= b + 0.1 for a, b in windows)]
         sm, mx, reasons, power = [], None, set(), []
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for r in rows:
             f = [x.strip() for x in r.split(",")]
             if len(f) < 9:
@@ -160,13 +177,13 @@ class ClockSampler:
                 power.append(float(f[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(self.NAMES, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+                "samples": len(sm), "sm_mhz_min": min(sm), "power_w_max": max(power) if power else None}
 
 
 # ------------------------------------------------------------ distributed
@@ -241,38 +258,415 @@ def host_data(projs):
     return out
 
 
-class GroupProjection:
-    """Several projections launched as one group: the bench's per-launch
-    figures (weight and algorithmic bytes, flops) summed over its members."""
+# ------------------------------------------------------------ device set-up
+class DeviceWorkload:
+    """One workload's operands resident in HBM and one plan per projection.
 
-    def __init__(self, members):
-        self.members = members
-        self.M = members[0].M
-        self.N = [p.N for p in members]
-        self.K = [p.K for p in members]
-        self.name = f"{members[0].name}..{members[-1].name}"
+    A step's activations (x, residual) and its outputs each live in one
+    packed buffer (256-byte aligned segments), so the end-to-end run moves
+    them with one host->device and one device->host copy per step.  Launch
+    arguments are kept as raw device addresses, so a launch costs the host
+    one call into the library."""
+
+    def __init__(self, name, dev, pdl=True, keep_host=False, host_bits=False):
+        import torch
+
+        from projection_gemm_gb300 import skg
+        from projection_gemm_gb300.inputs import bits, generate
+        self.name = name
+        self.projs, self.desc, self.cfg = workload(name)
+        gens = [generate(p) for p in self.projs]
+
+        def seg(nbytes):
+            return (nbytes + 255) // 256 * 256
+        in_bytes = sum(seg(t.x.numel() * 2) + (seg(t.res.numel() * 2) if t.res is not None else 0) for t in gens)
+        out_bytes = sum(seg(p.M * p.N * p.out_bytes_per_elem) for p in self.projs)
+        self.dev_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        self.dev_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+        host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        self.host_in = host_in if keep_host else None
+        self.host_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory() if keep_host else None
+
+        def view(buf, off, shape, dt):
+            n = shape[0] * shape[1] * torch.empty((), dtype=dt).element_size()
+            return buf[off:off + n].view(dt).view(*shape)
+
+        self.ops, self.host = [], []
+        oi = oo = 0
+        for p, t in zip(self.projs, gens):
+            if host_bits:
+                self.host.append((p, bits(t.x), bits(t.W), None if t.res is None else bits(t.res)))
+            plan = skg.Plan(p.M, p.N, p.K, p.epilogue)
+            plan.set_pdl(bool(pdl))
+            dt = torch.float32 if p.epilogue == "fp32" else torch.bfloat16
+            x = view(self.dev_in, oi, (p.M, p.K), torch.bfloat16)
+            view(host_in, oi, (p.M, p.K), torch.bfloat16).copy_(t.x)
+            oi += seg(t.x.numel() * 2)
+            res = None
+            if t.res is not None:
+                res = view(self.dev_in, oi, (p.M, p.N), torch.bfloat16)
+                view(host_in, oi, (p.M, p.N), torch.bfloat16).copy_(t.res)
+                oi += seg(t.res.numel() * 2)
+            y = view(self.dev_out, oo, (p.M, p.N), dt)
+            oo += seg(p.M * p.N * p.out_bytes_per_elem)
+            W = t.W.to(dev)
+            self.ops.append(dict(p=p, plan=plan, info=plan.info(), x=x, W=W, res=res, y=y,
+                                 args=(x.data_ptr(), W.data_ptr(), None if res is None else res.data_ptr(),
+                                       y.data_ptr())))
+        self.dev_in.copy_(host_in)
+        del gens
+        self.pools = None
 
     def weight_bytes(self):
-        return sum(p.weight_bytes() for p in self.members)
+        return sum(o["p"].weight_bytes() for o in self.ops)
 
-    def algorithmic_bytes(self):
-        return sum(p.algorithmic_bytes() for p in self.members)
+    def launch(self, o, s, W=None):
+        from projection_gemm_gb300 import skg
+        x, w, r, y = o["args"]
+        skg.skg_run(o["plan"].handle, x, w if W is None else W, r, y, s)
 
-    def flops(self):
-        return sum(p.flops() for p in self.members)
+    def step(self, s, events=None, at=None, side=None, side_join=True):
+        """One pass over every projection on stream handle `s`.  events: a
+        list of CUDA events recorded before the launches whose indices are in
+        `at` (all launches when `at` is None) and after the last one.  side:
+        (torch stream, its handle) on which each projection's successor gets
+        its L2 prefetch (skg_prefetch_l2) issued beside it."""
+        from projection_gemm_gb300 import skg
+        j = 0
+        n = len(self.ops)
+        for i, o in enumerate(self.ops):
+            if events is not None and (at is None or i in at):
+                events[j].record(self._streams[s])
+                j += 1
+            if side is not None and i + 1 < n:
+                if side_join:
+                    side[0].wait_stream(self._streams[s])
+                nx = self.ops[i + 1]
+                skg.skg_prefetch_l2(nx["plan"].handle, nx["args"][1], side[1])
+            self.launch(o, s)
+            if side is not None and side_join and i + 1 < n:
+                self._streams[s].wait_stream(side[0])
+        if side is not None and not side_join:
+            self._streams[s].wait_stream(side[0])
+        if events is not None:
+            events[j].record(self._streams[s])
+
+    def bind_streams(self, streams):
+        self._streams = {s.cuda_stream: s for s in streams}
+
+    def weight_pools(self, l2_bytes):
+        """Per (N, K): the workload's own weights of that shape, plus copies
+        until they hold at least twice the L2 (at least two)."""
+        if self.pools is None:
+            pools = {}
+            for o in self.ops:
+                pools.setdefault((o["p"].N, o["p"].K), []).append(o["W"])
+            for ws in pools.values():
+                i = 0
+                while len(ws) < 2 or sum(w.numel() * 2 for w in ws) < 2 * l2_bytes:
+                    ws.append(ws[i].clone())
+                    i += 1
+            self.pools = {k: [w.data_ptr() for w in ws] for k, ws in pools.items()}
+            self._pool_tensors = pools
+        return self.pools
+
+    def close(self):
+        for o in self.ops:
+            o["plan"].check()
+            o["plan"].close()
+        self.ops = []
+        self.pools = None
+        self._pool_tensors = None
 
 
-def make_group(members, ordered=True):
+def t_ideal_us(p, peak_hbm, peak_tf):
+    return max(p.algorithmic_bytes() / (peak_hbm * 1e9), p.flops() / (peak_tf * 1e12)) * 1e6
+
+
+def bar_for(p):
+    """The acceptance bar on a projection's roofline fraction: 0.80 for
+    M <= 16, 0.70 for M >= 32; PR1 (2 MB, below launch latency) has none."""
+    if p.name == "pr1":
+        return None
+    return 0.80 if p.M <= 16 else 0.70
+
+
+def measure_back_to_back(wl, s, torch_stream, l2_bytes, min_launches=28, reps=5):
+    """us per launch of each projection, launched alone back to back over
+    distinct weight copies.  The run is captured once as a CUDA graph (the
+    programmatic launch edges are kept) so that the host's launch rate never
+    limits it, and replayed `reps` times with events at its two ends."""
+    import torch
+    pools = wl.weight_pools(l2_bytes)
+    cap = torch.cuda.Stream(device=torch_stream.device)
+    out = []
+    for o in wl.ops:
+        pool = pools[(o["p"].N, o["p"].K)]
+        seq = pool * max(1, -(-min_launches // len(pool)))
+        cap.wait_stream(torch_stream)
+        with torch.cuda.stream(cap):
+            for w in seq:                           # eager once: first-use set-up outside the capture
+                wl.launch(o, cap.cuda_stream, W=w)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for w in seq:
+                wl.launch(o, cap.cuda_stream, W=w)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps + 1)]
+        for a, b in evs:
+            a.record(torch_stream)
+            g.replay()
+            b.record(torch_stream)
+        torch.cuda.synchronize()
+        t = [a.elapsed_time(b) * 1e3 / len(seq) for a, b in evs[1:]]
+        out.append((statistics.median(t), len(seq) * reps))
+        del g
+    return out
+
+
+def measure_event_isolated(wl, s, torch_stream, steps=24):
+    """us of each launch with events right before and after it, in whole
+    steps (median over the steps)."""
+    import torch
+    n = len(wl.ops)
+    per = [[] for _ in range(n)]
+    for _ in range(steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        wl.step(s, events=ev)
+        torch.cuda.synchronize()
+        for i in range(n):
+            per[i].append(ev[i].elapsed_time(ev[i + 1]) * 1e3)
+    return [statistics.median(v) for v in per]
+
+
+def measure_kind_runs(wl, s, torch_stream, steps=24):
+    """Each run of consecutive launches of one kernel kind inside whole
+    steps, events at the kind boundaries only: us per step per kind."""
+    import torch
+    runs, a = [], 0
+    for i in range(1, len(wl.ops) + 1):
+        if i == len(wl.ops) or wl.ops[i]["info"]["kernel"] != wl.ops[a]["info"]["kernel"]:
+            runs.append((a, i))
+            a = i
+    at = {r[0] for r in runs}
+    tot = {}
+    for _ in range(steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(runs) + 1)]
+        wl.step(s, events=ev, at=at)
+        torch.cuda.synchronize()
+        for j, (a, b) in enumerate(runs):
+            k = wl.ops[a]["info"]["kernel"]
+            d = tot.setdefault(k, {"launches_per_step": 0, "us": []})
+            d["us"].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+    for j, (a, b) in enumerate(runs):
+        k = wl.ops[a]["info"]["kernel"]
+        tot[k].setdefault("bytes_per_step", 0)
+        tot[k]["bytes_per_step"] += sum(wl.ops[i]["p"].algorithmic_bytes() for i in range(a, b))
+        tot[k]["launches_per_step"] += b - a
+    out = {}
+    for k, d in tot.items():
+        # one sample per step per run of this kind: sum the runs of a step
+        nr = sum(1 for a, b in runs if wl.ops[a]["info"]["kernel"] == k)
+        per_step = [sum(d["us"][i:i + nr]) for i in range(0, len(d["us"]), nr)]
+        us = statistics.median(per_step)
+        out[k] = {"launches_per_step": d["launches_per_step"], "bytes_per_step": d["bytes_per_step"],
+                  "us_per_step": round(us, 3), "gbs": round(d["bytes_per_step"] / us / 1e3, 1)}
+    return out
+
+
+def timed_pass(wl, s, torch_stream, steps, **kw):
+    """Device seconds of `steps` whole steps, events at the two ends only."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(torch_stream)
+    for _ in range(steps):
+        wl.step(s, **kw)
+    b.record(torch_stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3
+
+
+def projection_table(wl, b2b, iso, peak_hbm, peak_tf):
+    out = {}
+    for o, (us, launches), us_iso in zip(wl.ops, b2b, iso if iso else [None] * len(wl.ops)):
+        p, info = o["p"], o["info"]
+        ti = t_ideal_us(p, peak_hbm, peak_tf)
+        row = {"M": p.M, "N": p.N, "K": p.K, "epilogue": p.epilogue, "kernel": info["kernel"],
+               "split": info["split_k"], "grid": info["grid"], "stages": info["stages"],
+               "algorithmic_bytes": p.algorithmic_bytes(), "t_ideal_us": round(ti, 3),
+               "us_back_to_back": round(us, 3), "launches_timed": launches,
+               "weight_gbs": round(p.weight_bytes() / us / 1e3, 1),
+               "frac_back_to_back": round(ti / us, 4)}
+        if us_iso is not None:
+            row["us_event_isolated"] = round(us_iso, 3)
+            row["frac_event_isolated"] = round(ti / us_iso, 4)
+        bar = bar_for(p)
+        if bar is not None:
+            row["bar"] = bar
+            row["meets_bar"] = bool(ti / us >= bar)
+        out[p.name] = row
+    return out
+
+
+def roofline_from(table, wl, peak_hbm, peak_src, workload_name):
+    """The dominant kernel of the step (largest summed back-to-back time):
+    its projections' algorithmic bytes / their back-to-back time."""
+    kinds = {}
+    for o in wl.ops:
+        r = table[o["p"].name]
+        k = kinds.setdefault(r["kernel"], {"bytes": 0, "us": 0.0, "projections": []})
+        k["bytes"] += r["algorithmic_bytes"]
+        k["us"] += r["us_back_to_back"]
+        k["projections"].append(o["p"].name)
+    dom = max(kinds, key=lambda k: kinds[k]["us"])
+    d = kinds[dom]
+    achieved = d["bytes"] / (d["us"] * 1e-6) / 1e9
+    return {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak_hbm, "unit": "GB/s",
+            "frac": round(achieved / peak_hbm, 4), "traffic": kernel_traffic(dom, workload_name),
+            "peak_source": (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"),
+            "bytes_per_pass": d["bytes"], "us_per_pass": round(d["us"], 3), "projections": d["projections"],
+            "timing": ("achieved = bytes_per_pass / us_per_pass: the sum of this kernel's projections' algorithmic "
+                       "bytes over the sum of their us_back_to_back (per_projection), measured after the timed "
+                       "region")}
+
+
+def measure_config(name, dev, s, torch_stream, args, peak_hbm, peak_tf, l2_bytes, seconds=0.3):
+    """A named workload besides the headline: whole-step GB/s of a short
+    eager pass, and its per-projection figures."""
+    wl = DeviceWorkload(name, dev, pdl=bool(args.pdl))
+    wl.bind_streams([torch_stream])
+    try:
+        for _ in range(3):
+            wl.step(s)
+        t1 = timed_pass(wl, s, torch_stream, 1)
+        steps = max(5, min(400, int(seconds / max(t1, 1e-6))))
+        el = timed_pass(wl, s, torch_stream, steps)
+        b2b = measure_back_to_back(wl, s, torch_stream, l2_bytes)
+        iso = measure_event_isolated(wl, s, torch_stream, steps=12)
+        table = projection_table(wl, b2b, iso, peak_hbm, peak_tf)
+        out = {"workload": wl.desc, "steps": steps, "us_per_step": round(el / steps * 1e6, 3),
+               "gbs": round(wl.weight_bytes() * steps / el / 1e9, 1), "per_projection": table}
+        bars = [r for r in table.values() if "bar" in r]
+        out["projections_meeting_bar"] = f"{sum(r['meets_bar'] for r in bars)}/{len(bars)}"
+        if name == "chain":
+            out["variants"] = chain_variants(wl, s, torch_stream, steps, l2_bytes)
+        return out
+    finally:
+        wl.close()
+
+
+def chain_variants(wl, s, torch_stream, steps, l2_bytes):
+    """The chain end to end per M and in total, without prefetch, with the
+    in-launch prefetch of the next weight, and with skg_prefetch_l2 of the
+    next weight on a side stream (joined before the next projection, as the
+    pages' side stream is, and fire-and-forget with one join per step)."""
+    import torch
+    from projection_gemm_gb300 import inputs as I
+    side = torch.cuda.Stream(device=torch_stream.device)
+    wl.bind_streams([torch_stream, side])
+    per_m = len(I.CHAIN_STAGES)
+    seg_at = set(range(0, len(wl.ops), per_m))
+
+    def set_next(frac):
+        for i, o in enumerate(wl.ops):
+            if frac > 0 and (i + 1) % per_m != 0:
+                nx = wl.ops[i + 1]
+                o["plan"].set_next_weight(nx["W"], int(min(nx["p"].weight_bytes(), frac * l2_bytes)))
+            else:
+                o["plan"].set_next_weight(None, 0)
+
+    def one(label, frac=0.0, side_frac=None, join=True):
+        set_next(frac)
+        kw = {}
+        if side_frac is not None:
+            from projection_gemm_gb300 import skg
+            for o in wl.ops:
+                skg.skg_plan_set_prefetch_fraction(o["plan"].handle, side_frac)
+            kw = {"side": (side, side.cuda_stream), "side_join": join}
+        for _ in range(3):
+            wl.step(s, **kw)
+        el = timed_pass(wl, s, torch_stream, steps, **kw)
+        # per M: events at the M boundaries only
+        seg = [[] for _ in range(len(I.CHAIN_M))]
+        for _ in range(12):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(I.CHAIN_M) + 1)]
+            wl.step(s, events=ev, at=seg_at, **kw)
+            torch.cuda.synchronize()
+            for j in range(len(I.CHAIN_M)):
+                seg[j].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+        res = {"us_per_step": round(el / steps * 1e6, 3), "gbs": round(wl.weight_bytes() * steps / el / 1e9, 1),
+               "per_m": {}}
+        for j, m in enumerate(I.CHAIN_M):
+            us = statistics.median(seg[j])
+            wb = sum(o["p"].weight_bytes() for o in wl.ops[j * per_m:(j + 1) * per_m])
+            res["per_m"][f"m{m}"] = {"us": round(us, 3), "weight_gbs": round(wb / us / 1e3, 1)}
+        return label, res
+
+    out = dict([
+        one("no_prefetch"),
+        one("in_launch_next_weight_15pct_l2", frac=0.15),
+        one("side_stream_50pct_l2_joined", side_frac=0.5, join=True),
+        one("side_stream_15pct_l2_joined", side_frac=0.15, join=True),
+        one("side_stream_50pct_l2_unjoined", side_frac=0.5, join=False),
+    ])
+    set_next(0.0)
+    wl.bind_streams([torch_stream])
+    out["group_launch_per_m_ordered"] = chain_groups(wl, s, torch_stream, steps)
+    return out
+
+
+def chain_groups(wl, s, torch_stream, steps):
+    """The chain with each M's five projections as one group launch
+    (skg_group), each projection ordered after the previous one."""
+    import torch
+    from projection_gemm_gb300 import inputs as I
     from projection_gemm_gb300 import skg
-    ps = [o["p"] for o in members]
-    g = skg.Group(ps[0].M, [p.N for p in ps], [p.K for p in ps], [p.epilogue for p in ps],
-                  [0] + [1 if ordered else 0] * (len(ps) - 1))
-    info = g.info()
-    return dict(p=GroupProjection(ps), group=g, plans=[o["plan"] for o in members],
-                info={"kernel": "splitk_group", "split_k": info["split"], "prefetch_bytes": 0,
-                      "grid": info["grid"], "stages": info["stages"]},
-                x=[o["x"] for o in members], W=[o["W"] for o in members], res=[o["res"] for o in members],
-                y=[o["y"] for o in members])
+    per_m = len(I.CHAIN_STAGES)
+    groups = []
+    try:
+        for j, m in enumerate(I.CHAIN_M):
+            seg = wl.ops[j * per_m:(j + 1) * per_m]
+            g = skg.Group(m, [o["p"].N for o in seg], [o["p"].K for o in seg], [o["p"].epilogue for o in seg],
+                          [0] + [1] * (per_m - 1))
+            groups.append((g, [[o["args"][i] for o in seg] for i in range(4)]))
+
+        def step(events=None):
+            for j, (g, (xs, ws, rs, ys)) in enumerate(groups):
+                if events is not None:
+                    events[j].record(torch_stream)
+                skg.skg_group_run(g.handle, xs, ws, rs, ys, s)
+            if events is not None:
+                events[-1].record(torch_stream)
+        for _ in range(3):
+            step()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(torch_stream)
+        for _ in range(steps):
+            step()
+        b.record(torch_stream)
+        torch.cuda.synchronize()
+        el = a.elapsed_time(b) / 1e3
+        seg_us = [[] for _ in groups]
+        for _ in range(12):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(groups) + 1)]
+            step(ev)
+            torch.cuda.synchronize()
+            for j in range(len(groups)):
+                seg_us[j].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+        res = {"us_per_step": round(el / steps * 1e6, 3), "gbs": round(wl.weight_bytes() * steps / el / 1e9, 1),
+               "per_m": {}}
+        for j, m in enumerate(I.CHAIN_M):
+            us = statistics.median(seg_us[j])
+            wb = sum(o["p"].weight_bytes() for o in wl.ops[j * per_m:(j + 1) * per_m])
+            res["per_m"][f"m{m}"] = {"us": round(us, 3), "weight_gbs": round(wb / us / 1e3, 1),
+                                     "grid": groups[j][0].info()["grid"]}
+        for g, _ in groups:
+            g.check()
+        return res
+    finally:
+        for g, _ in groups:
+            g.close()
 
 
 # ---------------------------------------------------------------- our arm
@@ -281,7 +675,6 @@ def run_ours(args):
 
     from projection_gemm_gb300 import build as B
     from projection_gemm_gb300 import skg
-    from projection_gemm_gb300.inputs import generate
 
     rank, world, local = dist_env()
     if world > 1:
@@ -293,254 +686,102 @@ def run_ours(args):
     B.build()
     skg.load()
     dev = torch.device("cuda", torch.cuda.current_device())
-    projs, desc, cfg = workload(args.workload)
     peak_hbm, peak_tf, peak_src = load_peaks()
-
-    # Operands resident in HBM.  A step's activations (x, residual) and its
-    # outputs each live in one packed buffer (256-byte aligned segments), so
-    # the end-to-end run moves them with one host->device and one
-    # device->host copy per step.
-    def seg(nbytes):
-        return (nbytes + 255) // 256 * 256
-    gens = [generate(p) for p in projs]
-    in_bytes = sum(seg(t.x.numel() * 2) + (seg(t.res.numel() * 2) if t.res is not None else 0) for t in gens)
-    out_bytes = sum(seg(p.M * p.N * p.out_bytes_per_elem) for p in projs)
-    dev_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-    dev_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
-    host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-    host_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
-
-    def view(buf, off, shape, dt):
-        n = shape[0] * shape[1] * torch.empty((), dtype=dt).element_size()
-        return buf[off:off + n].view(dt).view(*shape)
-
-    ops, hostcopy = [], []
-    oi = oo = 0
-    for p, t in zip(projs, gens):
-        if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            from projection_gemm_gb300.inputs import bits
-            hostcopy.append((p, bits(t.x), bits(t.W), None if t.res is None else bits(t.res)))
-        plan = skg.Plan(p.M, p.N, p.K, p.epilogue)
-        plan.set_pdl(bool(args.pdl))
-        dt = torch.float32 if p.epilogue == "fp32" else torch.bfloat16
-        x = view(dev_in, oi, (p.M, p.K), torch.bfloat16)
-        view(host_in, oi, (p.M, p.K), torch.bfloat16).copy_(t.x)
-        oi += seg(t.x.numel() * 2)
-        res = None
-        if t.res is not None:
-            res = view(dev_in, oi, (p.M, p.N), torch.bfloat16)
-            view(host_in, oi, (p.M, p.N), torch.bfloat16).copy_(t.res)
-            oi += seg(t.res.numel() * 2)
-        y = view(dev_out, oo, (p.M, p.N), dt)
-        oo += seg(p.M * p.N * p.out_bytes_per_elem)
-        ops.append(dict(p=p, plan=plan, info=plan.info(), x=x, W=t.W.to(dev), res=res, y=y))
-    dev_in.copy_(host_in)
-    del gens
-    # [PF] on a side stream (--prefetch f): a prefetch kernel fills the L2
-    # with the next projection's weight while the current one runs.
-    side_pf = args.prefetch is not None and args.prefetch > 0
-    side = torch.cuda.Stream(device=dev)
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     stream = torch.cuda.current_stream(dev)
-    if args.prefetch is not None:
-        for o in ops:
-            skg.skg_plan_set_prefetch_fraction(o["plan"].handle, max(0.0, args.prefetch))
-
-    # [PF] inside the launch: each projection also asks the L2 for the first
-    # part of the weight that runs after it (the step wraps around).
-    next_frac = args.next_weight if args.next_weight is not None else (0.15 if args.workload == "chain" else 0.0)
-    if next_frac > 0:
-        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-        for i, o in enumerate(ops):
-            nxt = ops[(i + 1) % len(ops)]
-            o["plan"].set_next_weight(nxt["W"], int(min(nxt["p"].weight_bytes(), next_frac * l2)))
-
-    # --fused: each run of consecutive projections with the same M >= --fused-min-m is
-    # one group launch (skg_group), every projection after the first ordered
-    # after the previous one (dep), as consecutive launches are -- or, with
-    # --fused-order independent, with no order among them.
-    if args.fused:
-        side_pf = False
-        segs, i = [], 0
-        while i < len(ops):
-            j = i + 1
-            while ops[i]["p"].M >= args.fused_min_m and j < len(ops) and ops[j]["p"].M == ops[i]["p"].M:
-                j += 1
-            single = j == i + 1 and not (args.fused_single and ops[i]["p"].M >= args.fused_min_m)
-            segs.append(ops[i] if single else make_group(ops[i:j], args.fused_order == "chain"))
-            i = j
-        ops = segs
-
-    # Runs of consecutive launches of one kernel kind: events at their
-    # boundaries time each kind's launches without splitting the runs.
-    groups, g0 = [], 0
-    for i in range(1, len(ops) + 1):
-        if i == len(ops) or ops[i]["info"]["kernel"] != ops[g0]["info"]["kernel"]:
-            groups.append((g0, i))
-            g0 = i
-    group_start = {a: j for j, (a, _) in enumerate(groups)}
-
-    def launch(o, s):
-        if "group" in o:
-            o["group"].run(o["x"], o["W"], o["res"], o["y"], s)
-        else:
-            o["plan"].run(o["x"], o["W"], o["res"], o["y"], s)
-
-    def step(events=None, mode="launch", s=None):
-        s = stream if s is None else s
-        for i, o in enumerate(ops):
-            if side_pf and i + 1 < len(ops) and ops[i + 1]["info"]["prefetch_bytes"] > 0:
-                side.wait_stream(s)
-                ops[i + 1]["plan"].prefetch(ops[i + 1]["W"], side)
-            if events is not None and (mode == "launch" or i in group_start):
-                events[i if mode == "launch" else group_start[i]].record(s)
-            launch(o, s)
-            if side_pf and i + 1 < len(ops):
-                s.wait_stream(side)
-        if events is not None:
-            events[-1].record(s)
-
-    launches_per_step = len(ops) + (sum(1 for o in ops[1:] if o["info"]["prefetch_bytes"] > 0) if side_pf else 0)
-    wbytes_step = sum(o["p"].weight_bytes() for o in ops)
+    s = stream.cuda_stream
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    wl = DeviceWorkload(args.workload, dev, pdl=bool(args.pdl), keep_host=True, host_bits=want_cpu)
+    wl.bind_streams([stream])
+    launches_per_step = len(wl.ops)
+    wbytes_step = wl.weight_bytes()
 
     warm = max(3, args.warmup)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(warm):
-        step()
+        wl.step(s)
     torch.cuda.synchronize()
     est = (time.perf_counter() - t0) / warm
-    # --graph: a step's launches captured once into a CUDA graph (skg_run
-    # allocates nothing; the programmatic launch edges are kept, and a
-    # side-stream prefetch becomes a forked node joined before the next
-    # projection) and replayed each step, so the host issues one launch per
-    # step.  Steps that carry events run eagerly.
-    graph = None
-    if args.graph or (args.e2e_launch == "graph" and not args.no_e2e):
-        cap = torch.cuda.Stream(device=dev)
-        cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            step(s=cap)
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cap):
-            step(s=cap)   # the side stream forks from and joins back into the capture
-        side.wait_stream(stream)
-        torch.cuda.synchronize()
-        for _ in range(warm):
-            graph.replay()
-        torch.cuda.synchronize()
     K = args.steps if args.steps else max(20, min(40000, int(args.seconds / max(est, 1e-6))))
-    # Sampled steps carry events, alternately before every launch (the
-    # us/projection figures) or at kernel-kind boundaries only (each kind's
-    # launch durations, with the programmatic overlap inside a run intact).
-    # An event between two launches ends their overlap, so only about 300 of
-    # the K steps carry any.
-    sample_every = max(1, K // 300)
-    sampled = list(range(0, K, sample_every))
-    modes = {k: ("launch" if j % 2 == 0 else "group") for j, k in enumerate(sampled)}
-    evs = {k: [torch.cuda.Event(enable_timing=True)
-               for _ in range((len(ops) if modes[k] == "launch" else len(groups)) + 1)] for k in sampled}
 
     clocks = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
         if not args.no_clocks else None
     if clocks:
         clocks.start()
-        time.sleep(0.6)
+        time.sleep(0.5)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
+    # ---- timed region: exactly K steps, events only at its two ends
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     w0 = time.time()
     start.record(stream)
-    for k in range(K):
-        if args.graph and k not in evs:
-            graph.replay()
-        else:
-            step(evs.get(k), modes.get(k, "launch"))
+    for _ in range(K):
+        wl.step(s)
     end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
     if world > 1:
         dist.barrier()
-    if clocks:
-        time.sleep(0.3)
-        clocks.stop()
-        clocks.window(w0, w1)
     elapsed = start.elapsed_time(end) / 1e3
     max_t, total_bytes = aggregate(elapsed, wbytes_step * K, world)
     value = total_bytes / max_t / 1e9
 
-    # per-launch durations from the sampled steps (events on the launch stream)
-    per = {i: [] for i in range(len(ops))}
-    kern = {}
-    for k in sampled:
-        e = evs[k]
-        if modes[k] == "launch":
-            for i in range(len(ops)):
-                per[i].append(e[i].elapsed_time(e[i + 1]) * 1e3)  # us
-            continue
-        for j, (a, b) in enumerate(groups):
-            kk = kern.setdefault(ops[a]["info"]["kernel"], {"bytes": 0.0, "us": 0.0, "launches": 0})
-            kk["bytes"] += sum(ops[i]["p"].algorithmic_bytes() for i in range(a, b))
-            kk["us"] += e[j].elapsed_time(e[j + 1]) * 1e3
-            kk["launches"] += b - a
-    per_m = {}
-    for i, o in enumerate(ops):
-        p = o["p"]
-        us = statistics.median(per[i])
-        t_ideal = max(p.algorithmic_bytes() / (peak_hbm * 1e9), p.flops() / (peak_tf * 1e12)) * 1e6
-        key = f"{p.name}"
-        per_m[key] = {"M": p.M, "N": p.N, "K": p.K, "kernel": o["info"]["kernel"], "split": o["info"]["split_k"],
-                      "us": round(us, 3), "weight_gbs": round(p.weight_bytes() / us / 1e3, 1),
-                      "roofline_frac": round(t_ideal / us, 4)}
-        if "grid" in o["info"]:
-            per_m[key].update(grid=o["info"]["grid"], stages=o["info"]["stages"])
-    dom = max(kern, key=lambda k: kern[k]["us"])
-    achieved = kern[dom]["bytes"] / (kern[dom]["us"] * 1e-6) / 1e9
-    traffic = kernel_traffic(dom, args.workload)
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak_hbm, "unit": "GB/s",
-                "frac": round(achieved / peak_hbm, 4), "traffic": traffic,
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
-                "launches_timed": kern[dom]["launches"],
-                "timing": "events at the boundaries of each run of this kernel's launches in sampled steps"}
+    # ---- separate passes after the timed region
+    p0 = time.time()
+    b2b = measure_back_to_back(wl, s, stream, l2_bytes)
+    iso = measure_event_isolated(wl, s, stream)
+    table = projection_table(wl, b2b, iso, peak_hbm, peak_tf)
+    kinds = measure_kind_runs(wl, s, stream)
+    for k in kinds.values():
+        k["frac"] = round(k["gbs"] / peak_hbm, 4)
+    p1 = time.time()
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": warm, "ms_per_step": round(max_t / K * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": desc, **cfg, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "config": {"workload": wl.desc, **wl.cfg, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": ("inputs larger than L2: every step streams %.1f MB of distinct weights" % (wbytes_step / 1e6)),
-                   "pdl": bool(args.pdl),
-                   "fused_groups": bool(args.fused),
-                   **({"fused_order": ("each projection of a group after the previous one" if args.fused_order == "chain"
-                                       else "the projections of a group independent of one another"),
-                       "fused_min_m": args.fused_min_m}
-                      if args.fused else {}),
-                   "launch": ("cuda graph of the step's launches, replayed (steps carrying events run eagerly)"
-                              if args.graph else "eager skg_run calls"),
-                   "next_weight_l2_fraction": next_frac,
-                   "side_stream_prefetch_fraction": args.prefetch if side_pf else 0.0},
-        "per_projection": per_m, "roofline": roofline,
+                   "pdl": bool(args.pdl), "launch": "eager skg_run calls",
+                   "timed_region": "exactly `steps` steps, CUDA events only at its two ends"},
+        "per_projection": table,
+        "roofline": roofline_from(table, wl, peak_hbm, peak_src, args.workload),
+        "kernel_in_step": kinds,
         "gpu_launches": launches_per_step * K,
     }
-    if clocks:
-        result["clocks"] = clocks.summary()
+    bars = [r for r in table.values() if "bar" in r]
+    result["projections_meeting_bar"] = f"{sum(r['meets_bar'] for r in bars)}/{len(bars)}"
 
-    # e2e: activations from pinned host memory, outputs back, every step
+    # ---- e2e: activations from pinned host memory, outputs back, every step
     if not args.no_e2e:
+        graph = None
+        if args.e2e_launch == "graph":
+            cap = torch.cuda.Stream(device=dev)
+            cap.wait_stream(stream)
+            wl.bind_streams([stream, cap])
+            with torch.cuda.stream(cap):
+                wl.step(cap.cuda_stream)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=cap):
+                wl.step(cap.cuda_stream)
+            torch.cuda.synchronize()
+            wl.bind_streams([stream])
         Ke = max(3, min(K, int(args.e2e_seconds / max(est, 1e-6))))
-        h2d, d2h = host_in.numel(), host_out.numel()
+        h2d, d2h = wl.host_in.numel(), wl.host_out.numel()
 
         def e2e_step():
-            dev_in.copy_(host_in, non_blocking=True)
-            if args.e2e_launch == "graph":
+            wl.dev_in.copy_(wl.host_in, non_blocking=True)
+            if graph is not None:
                 graph.replay()
             else:
-                step()
-            host_out.copy_(dev_out, non_blocking=True)
+                wl.step(s)
+            wl.host_out.copy_(wl.dev_out, non_blocking=True)
             stream.synchronize()
-        for _ in range(2):
+        for _ in range(3):
             e2e_step()
         if world > 1:
             dist.barrier()
@@ -553,24 +794,38 @@ def run_ours(args):
                          "d2h_bytes_per_step": d2h, "steps": Ke,
                          "ms_per_step": round(te / Ke * 1e3, 4),
                          "launch": ("each step's skg_run calls captured once as a CUDA graph and replayed "
-                                    "between the copies" if args.e2e_launch == "graph" else
+                                    "between the copies" if graph is not None else
                                     "eager skg_run calls between the copies"),
                          "sync": "host waits for every step's output copy before the next step"}
+        del graph
 
-    for o in ops:
-        (o["group"] if "group" in o else o["plan"]).check()
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        smp = OracleSample(hostcopy, args.cpu_seconds)
+    host = wl.host
+    wl.close()
+    del wl
+    torch.cuda.empty_cache()
+
+    # ---- the other named workloads
+    c0 = time.time()
+    if not args.headline_only and rank == 0:
+        result["configs"] = {}
+        for name in EXTRA_CONFIGS:
+            if name == args.workload:
+                continue
+            result["configs"][name] = measure_config(name, dev, s, stream, args, peak_hbm, peak_tf, l2_bytes)
+            torch.cuda.empty_cache()
+    c1 = time.time()
+    if clocks:
+        time.sleep(0.2)
+        clocks.stop()
+        result["clocks"] = clocks.summary([(w0, w1), (p0, p1), (c0, c1)])
+        result["clocks"]["window"] = "timed region and the measurement passes after it"
+        result["clocks"]["samples_in_timed_region"] = clocks.summary([(w0, w1)])["samples"]
+
+    if want_cpu:
+        smp = OracleSample(host, args.cpu_seconds)
         gbs, secs = smp.run()
         result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": smp.cores, "kind": "oracle",
                                   "sample": smp.desc, "seconds": round(secs, 2)}
-    for o in ops:
-        if "group" in o:
-            o["group"].close()
-            for pl in o["plans"]:
-                pl.close()
-        else:
-            o["plan"].close()
     if world > 1:
         dist.destroy_process_group()
     return result if rank == 0 else None
@@ -617,26 +872,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--pdl", type=int, default=1)
-    ap.add_argument("--graph", type=int, default=0,
-                    help="1: replay each step as one captured CUDA graph (measured slower: replays do not overlap)")
     ap.add_argument("--e2e-launch", choices=("graph", "eager"), default="graph",
                     help="how the end-to-end leg issues a step's launches between its host copies")
-    ap.add_argument("--prefetch", type=float, default=None,
-                    help="fraction of L2 filled with the next weight by a kernel on a side stream (default: off)")
-    ap.add_argument("--next-weight", type=float, default=None,
-                    help="fraction of L2 of the next projection's weight each launch asks the L2 for "
-                         "(default: 0.15 for the chain, off otherwise)")
-    ap.add_argument("--fused", type=int, default=0,
-                    help="1: consecutive projections of one M (>= --fused-min-m) as one group launch (skg_group)")
-    ap.add_argument("--fused-order", choices=("chain", "independent"), default="chain",
-                    help="with --fused: order each projection after the previous one (as consecutive launches "
-                         "are), or run a group's projections as independent work (e.g. projections of one x)")
-    ap.add_argument("--fused-min-m", type=int, default=3,
-                    help="with --fused: the smallest M whose projections are grouped (M <= 2 groups run the "
-                         "split-K kernel, in place of the GEMV)")
-    ap.add_argument("--fused-single", type=int, default=0,
-                    help="with --fused: a projection with no same-M neighbour also runs as a "
-                         "one-projection group (units handed out dynamically)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other named workloads (wide, deep-K, PR1, chain)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define SKG_VERSION 1
+#define SKG_VERSION 2
 
 /* Symbols of the ABI are exported; everything else in the library is hidden. */
 #if defined(__GNUC__)
@@ -110,9 +110,6 @@ typedef struct skg_plan_desc {
     int l2_ahead;           /* weights requested into L2 ahead of use: TC k-blocks after the
                                ring, before the wait for the previous kernel; GEMV (split 1)
                                batches of the row; 0 = none */
-    int cluster_reduce;     /* TC: 1 = the split_k CTAs of a tile form a thread-block cluster and
-                               reduce through distributed shared memory (no workspace);
-                               0 = fp32 partials in the plan's workspace, last CTA reduces */
 } skg_plan_desc;
 
 typedef struct skg_plan_s *skg_plan_t;
@@ -135,9 +132,9 @@ SKG_API skg_status skg_plan_query(int M, int N, int K, int epilogue, int num_sms
 /*
  * skg_plan -- build a plan for (M,N,K,epilogue) on the current CUDA device.
  * Picks the kernel as skg_plan_query does and allocates a mapped host word for
- * device-side error reports; a tensor-core plan that reduces through its
- * global workspace (see skg_plan_set_reduction) also allocates S x ceil(N/128)
- * x M x 128 fp32 partials plus one zeroed counter per 128-row tile.  The plan must be
+ * device-side error reports; a tensor-core plan also allocates its split-K
+ * workspace, S x ceil(N/128) x M x 128 fp32 partials plus one zeroed
+ * counter per 128-row tile.  The plan must be
  * freed with skg_plan_destroy.  One skg_run of a plan may be in flight at a
  * time (the workspace is shared); concurrent streams need separate plans.
  * Errors: as skg_plan_query, plus SKG_ERR_CUDA.  *out is NULL on failure.
@@ -212,17 +209,6 @@ SKG_API skg_status skg_run(skg_plan_t plan, const void *x, const void *W,
 SKG_API skg_status skg_prefetch_l2(skg_plan_t next, const void *W_next, void *side_stream);
 
 /*
- * skg_plan_set_reduction -- how the split_k CTAs of a tensor-core plan combine
- * their partial sums: 0 (default) through the plan's global workspace and
- * the last-arriving CTA, so every other CTA leaves as soon as it has
- * written its partial; 1 through distributed shared memory inside a
- * thread-block cluster (no workspace, but all S CTAs stay until the slowest
- * arrives).  Both modes combine the partials in the same fixed order, so
- * they give the same bits.  GEMV plans: SKG_ERR_UNSUPPORTED.
- */
-SKG_API skg_status skg_plan_set_reduction(skg_plan_t plan, int cluster);
-
-/*
  * skg_plan_set_l2_ahead -- [PF] applied inside a kernel, without shared
  * memory or registers.  TC: before waiting for the previous kernel in the
  * stream, each CTA also requests the `ahead` weight tiles (128 x 64
@@ -270,7 +256,9 @@ SKG_API skg_status skg_plan_destroy(skg_plan_t plan);
  * waits on a shared-memory barrier that nothing ever arrives at, bounded by
  * timeout_ns of %globaltimer; on expiry the kernel records the timeout in
  * the plan's error word and returns normally, leaving the context usable.
- * A following skg_plan_check returns SKG_ERR_DEVICE_TIMEOUT.
+ * A following skg_plan_check returns SKG_ERR_DEVICE_TIMEOUT.  With plan
+ * NULL the timeout is recorded in the word of skg_run_noalloc's fixed array
+ * instead, and skg_noalloc_check reports it.
  */
 SKG_API skg_status skg_debug_wait_timeout(skg_plan_t plan, unsigned long long timeout_ns,
                                   void *stream);
@@ -280,26 +268,41 @@ SKG_API skg_status skg_debug_wait_timeout(skg_plan_t plan, unsigned long long ti
  * not allocate device memory: runtimes that own the whole device-memory
  * budget, code that must not enter the CUDA allocator, or hosts that cannot
  * create plans (skg_plan allocates).  It takes no plan, allocates nothing, and
- * keeps the kernel's fp32 partials and arrival counters in a fixed 16 MiB
- * array inside the library that every GPU loading the library holds until the
- * process exits.  The pages describe no such entry point; it exists only for
- * these callers.
+ * keeps the kernel's fp32 partials, arrival counters and timeout word in a
+ * fixed 16 MiB array inside the library that every GPU loading the library
+ * holds until the process exits.  The pages describe no such entry point; it
+ * exists only for these callers.
  *   M, N, K, epilogue, x, W, residual, y, stream: as for skg_plan + skg_run.
  *   Limits: M must be 3..64 (M <= 2 needs no scratch: use skg_run); the
- *   split's partials, split * M * N * 4 bytes, must fit 16 MiB - 64 KiB (the
- *   split is lowered to 2 if needed, else SKG_ERR_UNSUPPORTED); N at most
- *   16384 * 128.
+ *   partials at the picker's split, split * ceil(N/128) * 128 * M * 4 bytes,
+ *   must fit 16 MiB - 64 KiB - 256 bytes, else SKG_ERR_UNSUPPORTED (at
+ *   M = 64 that admits N up to 32512, where the picker splits K in 2).
  *   The first call on each device resolves the array's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   (cudaGetSymbolAddress) and keeps it for the life of the process: make
+ *   that first call before any stream capture, and do not reset the device
+ *   (cudaDeviceReset) after it.
  *   Every call clears the counters (cudaMemsetAsync on `stream`) and then
- *   launches one kernel; results are bit-identical to skg_run's.  All calls
- *   share the one array, so calls that overlap on the GPU (other streams, or
- *   other threads) race: serialise them.  A bounded wait that runs out stops
- *   the kernel but is not reported (there is no plan to hold an error word).
- * Errors: as skg_run.
+ *   launches one kernel, with the same L2 look-ahead as the plan path;
+ *   results are bit-identical to skg_run's.  All calls share the one array,
+ *   so calls that overlap on the GPU (other streams, or other threads) race:
+ *   serialise them.  A bounded wait that runs out stops the kernel, leaves y
+ *   incomplete and sets the array's timeout word, which skg_noalloc_check
+ *   reports.
+ * Errors: as skg_run, except that an earlier timeout is reported only by
+ * skg_noalloc_check.
  */
 SKG_API skg_status skg_run_noalloc(int M, int N, int K, int epilogue, const void *x, const void *W,
                                    const void *residual, void *y, void *stream);
+
+/*
+ * skg_noalloc_check -- synchronise `stream`, then report whether any kernel
+ * launched by skg_run_noalloc on the current device ran out of a bounded
+ * wait since the last check (SKG_ERR_DEVICE_TIMEOUT: the output of that call
+ * is incomplete; the word is then cleared), or a CUDA error is pending
+ * (SKG_ERR_CUDA).  Allocates nothing (a 4-byte device-to-host copy and, after
+ * a timeout, a 4-byte clear).
+ */
+SKG_API skg_status skg_noalloc_check(void *stream);
 
 /* Message of the last failed call on this thread ("" if none). */
 SKG_API const char *skg_last_error(void);

@@ -144,9 +144,7 @@ void fill_tc(skg_plan_desc *d, int split, int stages, int burst)
     d->tma_burst = std::max(1, std::min(burst, d->stages));
     const int n_tiles = (d->N + kTileN - 1) / kTileN;
     d->grid = n_tiles * split;
-    d->workspace_bytes = d->cluster_reduce ? 0
-                                           : tc_partial_bytes(d->M, d->N, split) +
-                                                 static_cast<size_t>(n_tiles) * sizeof(unsigned int);
+    d->workspace_bytes = tc_partial_bytes(d->M, d->N, split) + static_cast<size_t>(n_tiles) * sizeof(unsigned int);
 }
 
 const TableRow *table_lookup(int kind, int M, int N, int K, int epi)
@@ -250,9 +248,6 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
     } else {
         int split, stages = 0, burst = 1;
         const int n_tiles = (N + kTileN - 1) / kTileN;
-        // Measured: the workspace reduction frees early CTAs' SMs for the
-        // next kernel; a cluster holds all S CTAs until the slowest arrives.
-        d->cluster_reduce = 0;
         if (row) {
             split = row->split;
             stages = row->stages;
@@ -393,14 +388,9 @@ skg_status prepare_splitk_launch(int M, int N, int K, int epi, const void *x, co
     if (n_tiles > max_tiles)
         return fail(SKG_ERR_UNSUPPORTED, "N=%d needs %d arrival counters; the static scratch has %d", N, n_tiles,
                     max_tiles);
-    int split = d.split_k;
-    while (split > 2 && tc_partial_bytes(M, N, split) > scratch_bytes)
-        split /= 2;
-    if (tc_partial_bytes(M, N, split) > scratch_bytes)
-        return fail(SKG_ERR_UNSUPPORTED, "M*N=%lld needs %zu bytes of partials at split 2; the static scratch holds %zu",
-                    static_cast<long long>(M) * N, tc_partial_bytes(M, N, 2), scratch_bytes);
-    if (split != d.split_k)
-        fill_tc(&d, split, d.stages, d.tma_burst);
+    if (tc_partial_bytes(M, N, d.split_k) > scratch_bytes)
+        return fail(SKG_ERR_UNSUPPORTED, "M=%d N=%d needs %zu bytes of partials at split %d; the static scratch holds %zu",
+                    M, N, tc_partial_bytes(M, N, d.split_k), d.split_k, scratch_bytes);
     st = encode_2d(tmW, W, N, K, kTileN);
     if (st != SKG_OK)
         return st;
@@ -418,6 +408,7 @@ skg_status prepare_splitk_launch(int M, int N, int K, int epi, const void *x, co
     t->n_tiles = n_tiles;
     t->stages = d.stages;
     t->burst = d.tma_burst;
+    t->ahead = d.l2_ahead;
     t->epilogue = epi;
     t->timeout_ns = kDefaultTimeoutNs;
     *m_pad = d.m_pad;
@@ -568,15 +559,6 @@ skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out)
         delete p;
         return cuda_fail(e, "cudaHostGetDevicePointer(error word)");
     }
-    if (p->d.kernel_kind == SKG_KERNEL_SPLITK_TC && p->d.cluster_reduce) {
-        int clusters = 0;
-        e = tc_max_active_clusters(p->d.m_pad, p->d.stages, p->d.split_k, p->d.grid, &clusters);
-        if (e != cudaSuccess || clusters < 1) {
-            (void)cudaGetLastError();
-            p->d.cluster_reduce = 0;   // clusters of this size cannot be resident: reduce in memory
-            fill_tc(&p->d, p->d.split_k, p->d.stages, p->d.tma_burst);
-        }
-    }
     st = ensure_workspace(p);
     if (st != SKG_OK) {
         skg_plan_destroy(p);
@@ -716,27 +698,6 @@ skg_status skg_plan_set_l2_ahead(skg_plan_t p, int ahead)
     return SKG_OK;
 }
 
-skg_status skg_plan_set_reduction(skg_plan_t p, int cluster)
-{
-    if (!p)
-        return fail(SKG_ERR_INVALID_ARG, "skg_plan_set_reduction: plan is NULL");
-    if (p->d.kernel_kind != SKG_KERNEL_SPLITK_TC)
-        return fail(SKG_ERR_UNSUPPORTED, "only tensor-core plans split K across CTAs");
-    skg_plan_desc d = p->d;
-    d.cluster_reduce = cluster ? 1 : 0;
-    if (d.cluster_reduce) {
-        int clusters = 0;
-        cudaError_t e = tc_max_active_clusters(d.m_pad, d.stages, d.split_k, d.grid, &clusters);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
-        if (clusters < 1)
-            return fail(SKG_ERR_UNSUPPORTED, "clusters of %d CTAs cannot be resident for this plan", d.split_k);
-    }
-    fill_tc(&d, d.split_k, d.stages, d.tma_burst);
-    p->d = d;
-    return ensure_workspace(p);
-}
-
 skg_status skg_plan_set_prefetch_fraction(skg_plan_t p, double fraction)
 {
     if (!p)
@@ -825,7 +786,6 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         t.n_tiles = n_tiles;
         t.stages = d.stages;
         t.burst = d.tma_burst;
-        t.cluster = d.cluster_reduce ? d.split_k : 0;
         t.ahead = d.l2_ahead;
         t.next_w = static_cast<const unsigned char *>(p->next_w);
         t.next_bytes = p->next_bytes;
@@ -872,15 +832,23 @@ skg_status skg_plan_check(skg_plan_t p)
 
 skg_status skg_debug_wait_timeout(skg_plan_t p, unsigned long long timeout_ns, void *stream)
 {
-    if (!p)
-        return fail(SKG_ERR_INVALID_ARG, "skg_debug_wait_timeout: plan is NULL");
     if (timeout_ns == 0 || timeout_ns > 10000000000ull)
         return fail(SKG_ERR_INVALID_ARG, "timeout_ns must be in (0, 10 s]");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_debug_wait(p->err_dev, timeout_ns, s);
+    unsigned int *err = nullptr;
+    if (p) {
+        err = p->err_dev;
+    } else {
+        // no plan: the timeout word of skg_run_noalloc's fixed array
+        const skg_status st = noalloc_error_word(&err);
+        if (st != SKG_OK)
+            return st;
+    }
+    cudaError_t e = launch_debug_wait(err, timeout_ns, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "skg_debug_wait_timeout launch");
-    p->last_stream = s;
+    if (p)
+        p->last_stream = s;
     return SKG_OK;
 }
 

@@ -73,8 +73,6 @@ struct TcParams {
     int ahead;              // W tiles requested into L2 this many k-blocks ahead
     const unsigned char *next_w;  // the next projection's weight, or null
     size_t next_bytes;      // bytes of next_w the grid asks the L2 for (multiple of 16)
-    int cluster;            // S: the S CTAs of a tile form a cluster and reduce
-                            // through distributed shared memory; 0: workspace
     int epilogue;
     unsigned long long timeout_ns;
 };
@@ -168,8 +166,6 @@ cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, con
                              int m_pad, int grid, bool pdl, cudaStream_t s);
 cudaError_t launch_group_tc(const GroupParams &g, int m_pad, int grid, bool pdl, cudaStream_t s);
 int group_ctas_per_sm(int m_pad, int stages);   // co-resident CTAs of the group kernel
-// Clusters of `split` CTAs the tensor-core kernel can keep resident (0 if none).
-cudaError_t tc_max_active_clusters(int m_pad, int stages, int split, int grid, int *clusters);
 cudaError_t launch_prefetch_l2(const void *base, size_t bytes, cudaStream_t s);
 cudaError_t launch_debug_wait(unsigned int *err, unsigned long long timeout_ns, cudaStream_t s);
 // Records a failure message for skg_last_error and returns st.
@@ -177,8 +173,11 @@ skg_status set_error(skg_status st, const char *fmt, ...);
 
 // Everything one split-K launch needs, worked out on the host without
 // allocating: the checks of skg_run, the launch shape the picker chooses on
-// the current device (split lowered, if needed, until the partials fit
-// scratch_bytes), and the two TMA descriptors.  ws/counters are left null.
+// the current device (rejected if its partials do not fit scratch_bytes),
+// and the two TMA descriptors.  ws, counters and err are left null.
+// Device address of the timeout word in skg_run_noalloc's fixed array.
+skg_status noalloc_error_word(unsigned int **out);
+
 skg_status prepare_splitk_launch(int M, int N, int K, int epilogue, const void *x, const void *W,
                                  const void *residual, const void *y, size_t scratch_bytes,
                                  int max_tiles, CUtensorMap *tmW, CUtensorMap *tmX, TcParams *t,

@@ -47,45 +47,6 @@ namespace {
 
 #include "skg_tc_common.cuh"
 
-// Cluster mode: CTA `rank` of the tile's cluster produces rows
-// [rank * 128/S, (rank+1) * 128/S) of the tile for every column m, reading
-// the S subtree values from the S CTAs' shared memory in index order and
-// combining them by the top levels of the canonical tree (the same
-// arithmetic as the workspace reduction, so the same bits).
-template <int S, int MPAD>
-__device__ __forceinline__ void cluster_reduce(const TcParams &p, uint8_t *smem, int tile, int rank, int sp,
-                                               int et)
-{
-    constexpr int R = kTileN / S;
-    uint32_t base[S];
-    const uint32_t local = smem_u32(smem);
-#pragma unroll
-    for (int s = 0; s < S; ++s)
-        base[s] = map_shared_rank(local, static_cast<uint32_t>(s));
-    const int items = R * p.M;
-#pragma unroll 2
-    for (int i = et; i < items; i += kEpiThreads) {
-        const int m = i / R, rr = i - (i / R) * R;   // consecutive threads: consecutive rows
-        const int row = rank * R + rr;
-        const uint32_t off = static_cast<uint32_t>((row * (MPAD + 1) + m) * 4);
-        float v[S];
-#pragma unroll
-        for (int s = 0; s < S; ++s)
-            v[s] = (s < sp) ? ld_shared_cluster_f32(base[s] + off) : 0.f;
-#pragma unroll
-        for (int stride = 1; stride < S; stride <<= 1) {
-#pragma unroll
-            for (int j = 0; j + stride < S; j += 2 * stride) {
-                if (j + stride < sp)
-                    v[j] = v[j] + v[j + stride];
-            }
-        }
-        const int n = tile * kTileN + row;
-        if (n < p.N)
-            store_out(p, m, n, v[0]);
-    }
-}
-
 // Several CTAs share an SM (a short ring each): <= 102 registers per thread
 // for m_pad 48/64 (2 CTAs per SM), <= 68 for m_pad 16/32 (3 CTAs per SM).
 template <int MPAD>
@@ -112,9 +73,8 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort, [1] last
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // cluster mode: the S CTAs of a tile are consecutive (one cluster)
-    const int tile = p.cluster ? blockIdx.x / p.split : blockIdx.x % p.n_tiles;
-    const int split = p.cluster ? blockIdx.x % p.split : blockIdx.x / p.n_tiles;
+    const int tile = blockIdx.x % p.n_tiles;
+    const int split = blockIdx.x / p.n_tiles;
     const int L = kChunks / p.split;
     const int leaf0 = split * L;
     const int total_present = chunks_present(p.nkb);
@@ -328,17 +288,6 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                     }
                 }
             }
-            if (p.cluster) {
-                // this CTA's subtree into its own (now idle) ring memory,
-                // rows of m_pad + 1 floats so both access patterns are
-                // free of bank conflicts
-                if (present > 0) {
-                    float *part = reinterpret_cast<float *>(smem);
-#pragma unroll
-                    for (int c = 0; c < NC; ++c)
-                        part[row * (MPAD + 1) + half * NC + c] = cur[c];
-                }
-            } else {
             if (present > 0 && n < p.N) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
@@ -373,26 +322,7 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 if (ew == 0 && lane == 0)
                     p.counters[tile] = 0;
             }
-            }   // workspace mode
         }
-    }
-
-    if (p.cluster) {
-        // Every thread of every CTA of the cluster passes both barriers on
-        // every path (a skipped arrival would stall the peers).
-        __syncwarp();
-        cluster_sync();   // all partials written and visible
-        if (warp >= 2) {
-            const int sp = (total_present + L - 1) / L;
-            switch (p.split) {
-            case 2: cluster_reduce<2, MPAD>(p, smem, tile, split, sp, threadIdx.x - 64); break;
-            case 4: cluster_reduce<4, MPAD>(p, smem, tile, split, sp, threadIdx.x - 64); break;
-            case 8: cluster_reduce<8, MPAD>(p, smem, tile, split, sp, threadIdx.x - 64); break;
-            default: cluster_reduce<16, MPAD>(p, smem, tile, split, sp, threadIdx.x - 64); break;
-            }
-        }
-        __syncwarp();
-        cluster_sync();   // no CTA leaves while a peer still reads its memory
     }
 
     // Lane 0 of the producer and MMA warps ran their roles alone: reconverge
@@ -427,9 +357,6 @@ cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcPa
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
-        e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess)
-            return e;
         __atomic_store_n(&attr_set[dev], 232448, __ATOMIC_RELEASE);
     }
     cudaLaunchConfig_t cfg = {};
@@ -437,22 +364,11 @@ cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcPa
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    if (pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    if (p.cluster) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = na;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, splitk_tc_kernel<MPAD>, tmW, tmX, p);
 }
 
@@ -480,50 +396,6 @@ int tc_max_stages(int m_pad, int smem_limit)
     return s;
 }
 
-template <int MPAD>
-cudaError_t max_clusters_t(int stages, int split, int grid, int *clusters)
-{
-    // the attributes the launch sets (shared memory, cluster size) first
-    static int done[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    if (!__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) {
-        e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess)
-            return e;
-        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = tc_smem_bytes(MPAD, stages);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(clusters, splitk_tc_kernel<MPAD>, &cfg);
-}
-
-cudaError_t tc_max_active_clusters(int m_pad, int stages, int split, int grid, int *clusters)
-{
-    switch (m_pad) {
-    case 16: return max_clusters_t<16>(stages, split, grid, clusters);
-    case 32: return max_clusters_t<32>(stages, split, grid, clusters);
-    case 48: return max_clusters_t<48>(stages, split, grid, clusters);
-    case 64: return max_clusters_t<64>(stages, split, grid, clusters);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
 cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p,
                              int m_pad, int grid, bool pdl, cudaStream_t s)
 {
@@ -544,16 +416,23 @@ cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, con
 // A caller that may not allocate device memory (a runtime that owns the
 // whole memory budget, code running where the CUDA allocator must not be
 // entered, or a host that cannot create plans because plans allocate) can
-// still run the split-K kernel: its fp32 partials and arrival counters live
-// in the fixed array below, which every GPU that loads this library holds
-// until the process exits.
+// still run the split-K kernel: its fp32 partials, arrival counters and
+// timeout word live in the fixed array below, which every GPU that loads
+// this library holds until the process exits.
+//
+// Layout of the array: [0, 256) the timeout word (first 4 bytes) that the
+// kernels' bounded waits set and skg_noalloc_check reads and clears;
+// [256, 256 + 64 KiB) one arrival counter per 128-row tile; the rest, fp32
+// partials [split][tile][M][128].
 // ---------------------------------------------------------------------------
 namespace skg {
 namespace {
 
 constexpr size_t kScratchBytes = static_cast<size_t>(16) << 20;  // 16 MiB
+constexpr size_t kScratchErrBytes = 256;
 constexpr int kScratchTiles = 16384;                              // counters: N <= 2,097,152
 constexpr size_t kScratchCounterBytes = kScratchTiles * sizeof(unsigned int);
+constexpr size_t kScratchPartialBytes = kScratchBytes - kScratchErrBytes - kScratchCounterBytes;
 
 static __device__ __align__(256) unsigned char g_splitk_scratch[kScratchBytes];
 
@@ -561,7 +440,9 @@ std::mutex g_scratch_mutex;
 void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_splitk_scratch on the current device, looked up once
-// per device (the host-side name is only a stand-in for the symbol).
+// per device (the host-side name is only a stand-in for the symbol).  The
+// address is kept for the life of the process: a cudaDeviceReset after the
+// first call on a device is not supported.
 skg_status scratch_address(void **out)
 {
     int dev = 0;
@@ -584,6 +465,15 @@ skg_status scratch_address(void **out)
 
 } // namespace
 
+skg_status noalloc_error_word(unsigned int **out)
+{
+    void *scratch = nullptr;
+    const skg_status st = scratch_address(&scratch);
+    if (st == SKG_OK)
+        *out = static_cast<unsigned int *>(scratch);
+    return st;
+}
+
 } // namespace skg
 
 extern "C" skg_status skg_run_noalloc(int M, int N, int K, int epilogue, const void *x, const void *W,
@@ -597,20 +487,44 @@ extern "C" skg_status skg_run_noalloc(int M, int N, int K, int epilogue, const v
     CUtensorMap tmW, tmX;
     TcParams t;
     int m_pad = 0, grid = 0;
-    st = prepare_splitk_launch(M, N, K, epilogue, x, W, residual, y, kScratchBytes - kScratchCounterBytes,
-                               kScratchTiles, &tmW, &tmX, &t, &m_pad, &grid);
+    st = prepare_splitk_launch(M, N, K, epilogue, x, W, residual, y, kScratchPartialBytes, kScratchTiles, &tmW,
+                               &tmX, &t, &m_pad, &grid);
     if (st != SKG_OK)
         return st;
     unsigned char *base = static_cast<unsigned char *>(scratch);
-    t.counters = reinterpret_cast<unsigned int *>(base);
-    t.ws = reinterpret_cast<float *>(base + kScratchCounterBytes);
-    t.err = nullptr;   // no host-visible error word: a timed-out wait only stops the kernel
+    t.err = reinterpret_cast<unsigned int *>(base);
+    t.counters = reinterpret_cast<unsigned int *>(base + kScratchErrBytes);
+    t.ws = reinterpret_cast<float *>(base + kScratchErrBytes + kScratchCounterBytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: the counters must start at zero.
+    // The array keeps the previous call's contents: the counters must start at
+    // zero (the timeout word is left for skg_noalloc_check).
     cudaError_t e = cudaMemsetAsync(t.counters, 0, static_cast<size_t>(t.n_tiles) * sizeof(unsigned int), s);
     if (e == cudaSuccess)
         e = launch_splitk_tc(tmW, tmX, t, m_pad, grid, false, s);
     if (e != cudaSuccess)
         return set_error(SKG_ERR_CUDA, "skg_run_noalloc launch: %s", cudaGetErrorString(e));
+    return SKG_OK;
+}
+
+extern "C" skg_status skg_noalloc_check(void *stream)
+{
+    using namespace skg;
+    void *scratch = nullptr;
+    skg_status st = scratch_address(&scratch);
+    if (st != SKG_OK)
+        return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return set_error(SKG_ERR_CUDA, "skg_noalloc_check synchronize: %s", cudaGetErrorString(e));
+    unsigned int w = 0;
+    e = cudaMemcpy(&w, scratch, sizeof w, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && w != 0)
+        e = cudaMemset(scratch, 0, sizeof w);
+    if (e != cudaSuccess)
+        return set_error(SKG_ERR_CUDA, "skg_noalloc_check: %s", cudaGetErrorString(e));
+    if (w != 0)
+        return set_error(SKG_ERR_DEVICE_TIMEOUT,
+                         "a kernel of skg_run_noalloc ran out of a bounded wait (bits 0x%x); its output is incomplete",
+                         w);
     return SKG_OK;
 }

@@ -36,7 +36,7 @@ EXPORTS = (
     "skg_plan_query", "skg_plan", "skg_plan_force", "skg_plan_force_kernel", "skg_plan_set_pdl", "skg_run",
     "skg_prefetch_l2", "skg_plan_set_prefetch_fraction", "skg_plan_info", "skg_plan_check",
     "skg_plan_destroy", "skg_debug_wait_timeout", "skg_last_error", "skg_version",
-    "skg_run_noalloc", "skg_plan_set_reduction", "skg_plan_set_l2_ahead", "skg_plan_set_next_weight",
+    "skg_run_noalloc", "skg_noalloc_check", "skg_plan_set_l2_ahead", "skg_plan_set_next_weight",
     "skg_group", "skg_group_run", "skg_group_info", "skg_group_check", "skg_group_destroy",
 )
 
@@ -56,7 +56,6 @@ class skg_plan_desc(ctypes.Structure):
         ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
         ("from_table", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
         ("prefetch_bytes", ctypes.c_size_t), ("pdl", ctypes.c_int), ("l2_ahead", ctypes.c_int),
-        ("cluster_reduce", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -92,7 +91,7 @@ def load(path: str = LIB_PATH):
     lib.skg_plan_destroy.argtypes = [vp]
     lib.skg_debug_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, vp]
     lib.skg_run_noalloc.argtypes = [i, i, i, i, vp, vp, vp, vp, vp]
-    lib.skg_plan_set_reduction.argtypes = [vp, i]
+    lib.skg_noalloc_check.argtypes = [vp]
     lib.skg_plan_set_l2_ahead.argtypes = [vp, i]
     lib.skg_plan_set_next_weight.argtypes = [vp, vp, sz]
     lib.skg_group.argtypes = [i, i, P(i), P(i), P(i), P(i), P(vp)]
@@ -175,10 +174,6 @@ def skg_plan_set_l2_ahead(plan: int, ahead: int):
     _check(load().skg_plan_set_l2_ahead(plan, int(ahead)))
 
 
-def skg_plan_set_reduction(plan: int, cluster: bool):
-    _check(load().skg_plan_set_reduction(plan, 1 if cluster else 0))
-
-
 def skg_plan_set_prefetch_fraction(plan: int, fraction: float):
     _check(load().skg_plan_set_prefetch_fraction(plan, float(fraction)))
 
@@ -205,7 +200,8 @@ def skg_plan_destroy(plan: int):
     _check(load().skg_plan_destroy(plan))
 
 
-def skg_debug_wait_timeout(plan: int, timeout_ns: int, stream=None):
+def skg_debug_wait_timeout(plan, timeout_ns: int, stream=None):
+    """plan None: the timeout word of the allocation-free entry point."""
     _check(load().skg_debug_wait_timeout(plan, int(timeout_ns), _stream(stream)))
 
 
@@ -214,6 +210,12 @@ def skg_run_noalloc(M: int, N: int, K: int, epilogue, x, W, residual, y, stream=
     in-library scratch); see include/skg.h for its limits."""
     _check(load().skg_run_noalloc(M, N, K, _epi(epilogue), _ptr(x), _ptr(W), _ptr(residual), _ptr(y),
                                   _stream(stream)))
+
+
+def skg_noalloc_check(stream=None):
+    """Synchronise the stream; raise SKG_ERR_DEVICE_TIMEOUT if a kernel of
+    skg_run_noalloc ran out of a bounded wait since the last check."""
+    _check(load().skg_noalloc_check(_stream(stream)))
 
 
 class Plan:
@@ -241,9 +243,6 @@ class Plan:
 
     def set_l2_ahead(self, ahead: int):
         skg_plan_set_l2_ahead(self.handle, ahead)
-
-    def set_reduction(self, cluster: bool):
-        skg_plan_set_reduction(self.handle, cluster)
 
     def run(self, x, W, residual, y, stream=None):
         skg_run(self.handle, x, W, residual, y, stream)

@@ -69,10 +69,8 @@ def _group_case(M, shapes, dep, seed, runs=3):
         want = _single(M, N, K, epi, info["split"][i], xs[i], Ws[i], rs[i])
         assert np.array_equal(got[i], want), f"projection {i} ({K}->{N} {epi}) differs from skg_run"
         xb, wb, rb = bits(t.x), bits(t.W), None if t.res is None else bits(t.res)
-        rng = np.random.default_rng(seed + i)
-        ms, ns = rng.integers(0, M, 1500), rng.integers(0, N, 1500)
-        y_ref, s1 = O.linear_points(xb, wb, ms, ns, rb)
-        T.check(got[i][ms, ns], y_ref, s1, K, fp32=epi == "fp32", what=f"group projection {i}")
+        y_ref, s1, _ = O.linear(xb, wb, rb)
+        T.check(got[i], y_ref, s1, K, fp32=epi == "fp32", what=f"group projection {i} all outputs")
     return info
 
 
@@ -133,6 +131,12 @@ def test_dependent_chain_reads_the_previous_output(M):
                 got = out_bits(a)
                 assert not np.any((got & 0x7FFF) > 0x7F80), "NaN: a projection read its input too early"
                 assert np.array_equal(got, b)
+        # each stage against the oracle, fed the previous stage's GPU output
+        xin = bits(t0.x)
+        for i, (W, r, yb) in enumerate(zip((t0.W, t1.W, t2.W), (None, t1.res, None), want)):
+            y_ref, s1, _ = O.linear(xin, bits(W), None if r is None else bits(r))
+            T.check(yb, y_ref, s1, xin.shape[1], what=f"dependent group stage {i}")
+            xin = yb
     finally:
         g.close()
 
@@ -159,6 +163,9 @@ def test_group_captures_into_a_cuda_graph():
         torch.cuda.synchronize()
         g.check()
         assert all(np.array_equal(out_bits(y), w) for y, w in zip(ys, want))
+        for i, ((K, N, epi), t) in enumerate(zip(shapes, ts)):
+            y_ref, s1, _ = O.linear(bits(t.x), bits(t.W), None if t.res is None else bits(t.res))
+            T.check(out_bits(ys[i]), y_ref, s1, K, what=f"graph-replayed group projection {i}")
     finally:
         g.close()
 

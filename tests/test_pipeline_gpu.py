@@ -14,8 +14,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle.oracle as O
 from projection_gemm_gb300 import skg
-from projection_gemm_gb300.inputs import Projection, generate
+from projection_gemm_gb300.inputs import Projection, bits, generate
+from tests import tolerance as T
 from tests.gpu_util import out_bits, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -26,6 +28,29 @@ def _lib():
     from projection_gemm_gb300 import build
     build.build()
     skg.load()
+
+
+class Reference:
+    """The oracle's values for one projection's operands (computed once),
+    and the acceptance check of a GPU output against them."""
+
+    def __init__(self, x, W, res=None, fp32=False):
+        self.K = x.shape[1]
+        self.fp32 = fp32
+        self.y, self.s1, _ = O.linear(bits(x.cpu()), bits(W.cpu()), None if res is None else bits(res.cpu()))
+
+    def check(self, y_bits, what):
+        T.check(y_bits, self.y, self.s1, self.K, fp32=self.fp32, what=what)
+
+
+def check_chain(x0, Ws, y_bits, what):
+    """Each stage of a chain against the oracle, fed the bits the GPU's
+    previous stage produced."""
+    x = bits(x0.cpu())
+    for i, (W, yb) in enumerate(zip(Ws, y_bits)):
+        y_ref, s1, _ = O.linear(x, bits(W.cpu()))
+        T.check(yb, y_ref, s1, x.shape[1], what=f"{what} stage {i}")
+        x = yb
 
 
 def _chain_run(plans, Ws, x0, ys, pdl: bool, serialize: bool):
@@ -59,6 +84,7 @@ def test_pdl_chain_reads_activations_after_wait(M):
         ref = _chain_run(plans, Ws, x0, ys, pdl=False, serialize=True)
         for a in ref:
             assert not np.any((a & 0x7FFF) > 0x7F80), "NaN in the serialised chain"
+        check_chain(x0, Ws, ref, f"M={M} serialised chain")
         for _ in range(10):
             got = _chain_run(plans, Ws, x0, ys, pdl=True, serialize=False)
             for a, b in zip(got, ref):
@@ -83,16 +109,24 @@ def test_prefetch_beside_projection(M):
         p_next.run(x2, W2, None, y2)
         torch.cuda.synchronize()
         ref, ref2 = out_bits(y), out_bits(y2)
+        want, want2 = Reference(x, W), Reference(x2, W2)
         side = torch.cuda.Stream()
         main = torch.cuda.current_stream()
-        for _ in range(5):
-            side.wait_stream(main)
-            p_next.prefetch(W2, side)
-            p_cur.run(x, W, None, y)
+        for joined in (True, False):
+            for y_ in (y, y2):
+                y_.view(torch.int16).fill_(0x7FC0)
+            for _ in range(5):
+                side.wait_stream(main)
+                p_next.prefetch(W2, side)
+                p_cur.run(x, W, None, y)
+                if joined:                       # the next projection after its prefetch
+                    main.wait_stream(side)
+                p_next.run(x2, W2, None, y2)
             main.wait_stream(side)
-            p_next.run(x2, W2, None, y2)
-        torch.cuda.synchronize()
-        assert np.array_equal(out_bits(y), ref) and np.array_equal(out_bits(y2), ref2)
+            torch.cuda.synchronize()
+            want.check(out_bits(y), f"M={M} beside the prefetch (joined={joined})")
+            want2.check(out_bits(y2), f"M={M} after its prefetch (joined={joined})")
+            assert np.array_equal(out_bits(y), ref) and np.array_equal(out_bits(y2), ref2)
         skg.skg_plan_set_prefetch_fraction(p_next.handle, 0.0)
         assert p_next.info()["prefetch_bytes"] == 0
         p_next.prefetch(W2, side)
@@ -129,7 +163,9 @@ def test_graph_capture_of_a_chain():
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
-        for a, b in zip([out_bits(y) for y in ys], ref):
+        got = [out_bits(y) for y in ys]
+        check_chain(x0, Ws, got, "graph replay")
+        for a, b in zip(got, ref):
             assert np.array_equal(a, b)
     finally:
         for p in plans:
@@ -152,13 +188,18 @@ def test_next_weight_prefetch_inside_the_launch(M):
         p_next.run(x2, W2, r2, y2)
         torch.cuda.synchronize()
         ref, ref2 = out_bits(y), out_bits(y2)
+        want, want2 = Reference(x, W), Reference(x2, W2, r2)
         for nbytes in (16, 1 << 20, 2 * 4096 * 7168, 1 << 40):   # capped at the L2 size
             p_cur.set_next_weight(W2, nbytes)
             p_next.set_next_weight(W, nbytes)
+            for y_ in (y, y2):
+                y_.view(torch.int16).fill_(0x7FC0)
             for _ in range(3):
                 p_cur.run(x, W, None, y)
                 p_next.run(x2, W2, r2, y2)
             torch.cuda.synchronize()
+            want.check(out_bits(y), f"M={M} prefetching {nbytes} bytes of the next weight")
+            want2.check(out_bits(y2), f"M={M} after the in-launch prefetch of {nbytes} bytes")
             assert np.array_equal(out_bits(y), ref) and np.array_equal(out_bits(y2), ref2), nbytes
         with pytest.raises(skg.SkgError) as e:
             p_cur.set_next_weight(W2.data_ptr() + 2, 1 << 20)
