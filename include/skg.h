@@ -216,7 +216,7 @@ SKG_API skg_status skg_prefetch_l2(skg_plan_t next, const void *W_next, void *si
  * keeps HBM busy with this launch's weights.  GEMV split 1 with 16-byte
  * loads (stages 0) or in one wave (stages 3): each batch is also requested
  * into L2 `ahead` batches before it is loaded (the first ones before the
- * wait).  0..16; 0 turns it off.  The GEMV ring kernel (split > 1) and the
+ * wait).  0..64; 0 turns it off.  The GEMV ring kernel (split > 1) and the
  * whole-row bulk-copy form (stages 2) ignore it.
  */
 SKG_API skg_status skg_plan_set_l2_ahead(skg_plan_t plan, int ahead);

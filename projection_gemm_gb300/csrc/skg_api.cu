@@ -341,6 +341,18 @@ struct MapCache {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The last two arrivals of a tile share its reduction at M > 16, where the
+// partials take a last CTA two rounds of loads (measured on GB300: 1 to 2 us
+// saved per launch at M = 64; at M <= 16 the wait costs more than it saves).
+// Safe only when at most one CTA per tile waits and the waiters cannot fill
+// the SMs: every other CTA of the grid runs to completion without waiting,
+// so the CTA a waiter waits for always gets an SM.  Splits of 16 reduce in
+// one CTA (per-row form).
+int pair_reduce_ok(int M, int n_tiles, int split, int num_sms)
+{
+    return (M > 16 && split <= 8 && n_tiles < num_sms) ? 1 : 0;
+}
+
 } // namespace
 
 namespace skg {
@@ -411,6 +423,7 @@ skg_status prepare_splitk_launch(int M, int N, int K, int epi, const void *x, co
     t->ahead = d.l2_ahead;
     t->epilogue = epi;
     t->timeout_ns = kDefaultTimeoutNs;
+    t->pair_reduce = pair_reduce_ok(M, n_tiles, d.split_k, sms);
     *m_pad = d.m_pad;
     *grid = d.grid;
     return SKG_OK;
@@ -692,8 +705,8 @@ skg_status skg_plan_set_l2_ahead(skg_plan_t p, int ahead)
 {
     if (!p)
         return fail(SKG_ERR_INVALID_ARG, "skg_plan_set_l2_ahead: plan is NULL");
-    if (ahead < 0 || ahead > 16)
-        return fail(SKG_ERR_INVALID_ARG, "ahead=%d outside 0..16", ahead);
+    if (ahead < 0 || ahead > 64)
+        return fail(SKG_ERR_INVALID_ARG, "ahead=%d outside 0..64", ahead);
     p->d.l2_ahead = ahead;
     return SKG_OK;
 }
@@ -791,6 +804,7 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         t.next_bytes = p->next_bytes;
         t.epilogue = d.epilogue;
         t.timeout_ns = kDefaultTimeoutNs;
+        t.pair_reduce = pair_reduce_ok(d.M, n_tiles, d.split_k, p->num_sms);
         e = launch_splitk_tc(*mw, *mx, t, d.m_pad, d.grid, d.pdl != 0, s);
     }
     if (e != cudaSuccess)

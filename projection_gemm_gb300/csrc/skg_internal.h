@@ -75,6 +75,7 @@ struct TcParams {
     size_t next_bytes;      // bytes of next_w the grid asks the L2 for (multiple of 16)
     int epilogue;
     unsigned long long timeout_ns;
+    int pair_reduce;        // 1: the last two arrivals of a tile each reduce half of it
 };
 
 // Several projections of the same M in one persistent split-K launch.

@@ -47,6 +47,26 @@ namespace {
 
 #include "skg_tc_common.cuh"
 
+// Second-to-last arrival of a tile: poll the tile's counter (acquire, GPU
+// scope) until all `target` arrivals are in, for at most timeout_ns, or until
+// another role of the CTA gave up.  The CTA it waits for belongs to the same
+// grid and never waits itself, and at most one CTA per tile waits, so the
+// host enables this only while the tiles are fewer than the SMs.
+__device__ __forceinline__ bool wait_arrivals(const unsigned *ctr, unsigned target, uint64_t timeout_ns,
+                                              volatile int *abort)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if ((v & 0xFFFFu) >= target)
+            return true;
+        if (*abort || globaltimer_ns() - t0 > timeout_ns)
+            return false;
+        __nanosleep(32);
+    }
+}
+
 // Several CTAs share an SM (a short ring each): <= 102 registers per thread
 // for m_pad 48/64 (2 CTAs per SM), <= 68 for m_pad 16/32 (3 CTAs per SM).
 template <int MPAD>
@@ -227,6 +247,11 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         const uint32_t lvl2 = lane_base + 3 * MPAD;
         float st0[NC], cur[NC];
         bool ok = true;
+        // Canonical tree over this CTA's chunks, as a binary counter: chunk
+        // pl closes the blocks of 2, 4 and 8 chunks that end with it.  Level
+        // 0 waits in registers, levels 1 and 2 in spare TMEM columns.  After
+        // the last chunk cur holds the block of the lowest set bit of
+        // `present`; only blocks that a later chunk still needs are stored.
         for (int pl = 0; pl < present; ++pl) {
             const int b = pl & 1;
             const uint32_t u = static_cast<uint32_t>(pl >> 1);
@@ -241,53 +266,33 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&tempty[b]);
-            // canonical tree over this CTA's chunks: merge completed pairs.
-            // Level 0 stays in registers, levels 1 and 2 in spare TMEM columns.
+            const bool more = pl + 1 < present;
             if (pl & 1) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) cur[c] = st0[c] + cur[c];
                 if (pl & 2) {
                     tmem_add_cols<NC>(lvl1, cur);
-                    if (pl & 4) {
+                    if (pl & 4)
                         tmem_add_cols<NC>(lvl2, cur);
-                    } else {
+                    else if (more)
                         tmem_store_cols<NC>(lvl2, cur);
-                    }
-                } else {
+                } else if (more) {
                     tmem_store_cols<NC>(lvl1, cur);
                 }
-            } else {
+            } else if (more) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) st0[c] = cur[c];
             }
         }
         ok = epi_bar_and(ok && !flags[0]);
         if (ok) {
-            // value of the subtree: 8 chunks -> cur; else fold the stored
-            // complete blocks from the smallest upwards
-            if (present != 8 && present > 0) {
-                bool have = false;
-                if (present & 1) {
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) cur[c] = st0[c];
-                    have = true;
-                }
-                if (present & 2) {
-                    if (have) {
-                        tmem_add_cols<NC>(lvl1, cur);
-                    } else {
-                        tmem_load_cols<NC>(lvl1, cur);
-                    }
-                    have = true;
-                }
-                if (present & 4) {
-                    if (have) {
-                        tmem_add_cols<NC>(lvl2, cur);
-                    } else {
-                        tmem_load_cols<NC>(lvl2, cur);
-                    }
-                }
-            }
+            // The subtree's value: the stored larger blocks folded onto cur,
+            // smallest first (the left operand is the earlier block).
+            const int low = present & -present;
+            if ((present & 2) && low < 2)
+                tmem_add_cols<NC>(lvl1, cur);
+            if ((present & 4) && low < 4)
+                tmem_add_cols<NC>(lvl2, cur);
             if (present > 0 && n < p.N) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
@@ -301,26 +306,53 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             // scope; the last arriver's acquire, passed on by the next
             // barrier, orders its reads of all partials after the stores.
             epi_bar_sync();
+            const bool pair = p.pair_reduce && p.split <= 8;
             if (ew == 0 && lane == 0) {
-                const unsigned old = atom_add_acq_rel_gpu(&p.counters[tile], 1u);
-                flags[1] = (old == static_cast<unsigned>(p.split - 1)) ? 1 : 0;
+                // Low 16 bits of the tile's counter: arrivals; high bits:
+                // reducers that have seen every arrival.
+                const unsigned old = atom_add_acq_rel_gpu(&p.counters[tile], 1u) & 0xFFFFu;
+                int role = 0;
+                if (old == static_cast<unsigned>(p.split - 1)) {
+                    role = 1;                    // last arrival
+                } else if (pair && old == static_cast<unsigned>(p.split - 2)) {
+                    // second to last: wait (bounded) for the last arrival,
+                    // then reduce the first half of the tile's outputs
+                    if (wait_arrivals(&p.counters[tile], static_cast<unsigned>(p.split), p.timeout_ns, &flags[0]))
+                        role = 2;
+                    else
+                        record_failure(p, &flags[0], kErrTimeoutEpilogue);
+                }
+                if (role && pair) {
+                    // the second reducer to get here has seen both see every
+                    // arrival: it returns the counter to zero
+                    if ((atom_add_acq_rel_gpu(&p.counters[tile], 1u << 16) >> 16) == 1)
+                        p.counters[tile] = 0;
+                } else if (role) {
+                    p.counters[tile] = 0;
+                }
+                flags[1] = role;
             }
             epi_bar_sync();
-            if (flags[1]) {
+            const int role = flags[1];
+            if (role) {
                 const int sp = (total_present + L - 1) / L;  // splits holding a value
                 const int et = threadIdx.x - 64;
+                // outputs of the tile in work items; with pair_reduce the last
+                // arrival takes the second half, the one before it the first
+                const int items = p.M * (kTileN / 4);
+                const int mid = pair ? (items / 2 + 31) / 32 * 32 : 0;
+                const int i0 = role == 2 ? 0 : mid;
+                const int i1 = role == 2 ? mid : items;
                 constexpr int kL = MPAD <= 32 ? 8 : 16;   // 16-byte loads in flight per thread
                 switch (p.split) {
-                case 2: reduce_tile_v4<2, kL>(p, tile, sp, et); break;
-                case 4: reduce_tile_v4<4, kL>(p, tile, sp, et); break;
-                case 8: reduce_tile_v4<8, kL>(p, tile, sp, et); break;
+                case 2: reduce_tile_v4<2, kL>(p, tile, sp, et, i0, i1); break;
+                case 4: reduce_tile_v4<4, kL>(p, tile, sp, et, i0, i1); break;
+                case 8: reduce_tile_v4<8, kL>(p, tile, sp, et, i0, i1); break;
                 default:
                     if (n < p.N)
                         reduce_tile<16, NC>(p, tile, row, half, sp);
                     break;
                 }
-                if (ew == 0 && lane == 0)
-                    p.counters[tile] = 0;
             }
         }
     }

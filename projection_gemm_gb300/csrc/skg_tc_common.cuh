@@ -169,8 +169,9 @@ __device__ __forceinline__ void reduce_tile(const PP &p, int tile, int row, int 
 // 4g..4g+3 of column m, so the 32 lanes of a warp read 512 contiguous bytes
 // of each split's block, and each output is combined exactly as in
 // reduce_tile (the top levels of the canonical tree, in index order).  The
-// 256 epilogue threads take items et, et + 256, ...; IB = L / S items per
-// batch keep L loads in flight (L as the CTA shape's register budget allows).
+// 256 epilogue threads take items i_begin + et, + 256, ... below i_end (all
+// items by default); IB = L / S items per batch keep L loads in flight (L as
+// the CTA shape's register budget allows).
 template <class PP>
 __device__ __forceinline__ void store_out4(const PP &p, int m, int n0, int cnt, const float4 &v)
 {
@@ -202,15 +203,16 @@ __device__ __forceinline__ void store_out4(const PP &p, int m, int n0, int cnt, 
 }
 
 template <int S, int L, class PP>
-__device__ __forceinline__ void reduce_tile_v4(const PP &p, int tile, int sp, int et)
+__device__ __forceinline__ void reduce_tile_v4(const PP &p, int tile, int sp, int et, int i_begin = 0,
+                                               int i_end = -1)
 {
     constexpr int IB = S >= L ? 1 : L / S;        // items per batch
     const int rows = min(kTileN, p.N - tile * kTileN);
-    const int items = p.M * (kTileN / 4);
+    const int items = i_end < 0 ? p.M * (kTileN / 4) : i_end;
     const float *base = p.ws + static_cast<size_t>(tile) * p.M * kTileN;
     const size_t sstride = static_cast<size_t>(p.n_tiles) * p.M * kTileN;
 #pragma unroll 1
-    for (int i0 = et; i0 < items; i0 += kEpiThreads * IB) {
+    for (int i0 = i_begin + et; i0 < items; i0 += kEpiThreads * IB) {
         float4 v[IB][S];
 #pragma unroll
         for (int b = 0; b < IB; ++b) {
@@ -245,4 +247,3 @@ __device__ __forceinline__ void reduce_tile_v4(const PP &p, int tile, int sp, in
         }
     }
 }
-

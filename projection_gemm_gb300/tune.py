@@ -55,8 +55,10 @@ def candidates(M, N, K):
         c += [{"kind": skg.SKG_KERNEL_SPLITK_TC, "split_k": sp, "stages": st, "ahead": a}
               for sp in (2, 4, 8) for st in (4, 5, 6) for a in (0, 2)]
         return c
+    # ahead up to a CTA's whole K range: the next launch's weight requests
+    # can cover the previous launch's tail
     return [{"split_k": s, "stages": st, "ahead": a} for s in (2, 4, 8, 16) for st in (3, 4, 5, 6)
-            for a in (0, 2, 4, 6, 8)]
+            for a in (0, 2, 4, 8, 12, 16, 24, 32)]
 
 
 def read_rows(path):

@@ -138,7 +138,7 @@ def test_plan_table_rows_are_well_formed():
         if kind == skg.SKG_KERNEL_GEMV:
             assert M <= 2 and split <= 8
         else:
-            assert split >= 2 and 2 <= stages <= 16 and burst >= 1 and 0 <= ahead <= 16
+            assert split >= 2 and 2 <= stages <= 16 and burst >= 1 and 0 <= ahead <= 64
         assert us > 0 and 0 < gbs < 8000          # no launch streams faster than the HBM
         epi_name = {0: "bf16", 1: "bf16_residual", 2: "fp32"}[epi]
         d = skg.skg_plan_query(M, N, K, epi_name, SMS, L2)
