@@ -173,6 +173,36 @@ SKG_API skg_status skg_plan_force(skg_plan_t plan, int split_k, int stages, int 
 SKG_API skg_status skg_plan_force_kernel(skg_plan_t plan, int kind);
 
 /*
+ * skg_plan_set_k_shard -- [OC] row-parallel projection: the plan computes
+ * rank `rank` of `ranks` (1, 2, 4 or 8) of a K split across ranks.  Rank r
+ * owns canonical chunks [16r/R, 16(r+1)/R) of K, i.e. columns [rK/R,
+ * (r+1)K/R) (K % 1024 == 0 when ranks > 1).  After this call skg_run takes
+ * x as that shard [M, K/R] and W as [N, K/R] (dense, row stride K/R) and
+ * leaves in y (fp32 [M, N]: the plan's epilogue must be SKG_EPI_FP32) the
+ * value of the rank's subtree of the canonical tree, so that
+ * skg_combine_partials over the R ranks gives exactly the bits of one
+ * launch of the split-K kernel over the whole K.  The plan switches to the
+ * split-K kernel if needed and splits a rank's chunks at most 16/R ways;
+ * skg_prefetch_l2 then covers the shard.  ranks == 1 restores the whole K.
+ * Errors: SKG_ERR_INVALID_ARG, SKG_ERR_UNSUPPORTED (epilogue, K), SKG_ERR_CUDA.
+ */
+SKG_API skg_status skg_plan_set_k_shard(skg_plan_t plan, int rank, int ranks);
+
+/*
+ * skg_combine_partials -- the cross-rank step of a row-parallel projection
+ * [OC]: y[m,n] = the R rank partials (fp32 [M, N] each; `partials` is a host
+ * array of R device pointers) combined in rank order by the top levels of
+ * the canonical tree, + residual (bf16 [M, N], given iff epilogue is
+ * SKG_EPI_BF16_RESIDUAL) in fp32, rounded once to bf16 (stored as fp32 for
+ * SKG_EPI_FP32).  The caller brings the partials to this device first (an
+ * all-gather, or peer pointers).  ranks: 1, 2, 4 or 8.  One kernel on
+ * `stream`; allocates nothing.
+ * Errors: SKG_ERR_INVALID_ARG, SKG_ERR_ALIGNMENT, SKG_ERR_CUDA.
+ */
+SKG_API skg_status skg_combine_partials(int M, int N, int ranks, const float *const *partials,
+                                        const void *residual, void *y, int epilogue, void *stream);
+
+/*
  * skg_plan_set_pdl -- 1 (default): launch with programmatic dependent launch,
  * so a kernel's prologue and its first WEIGHT loads overlap the previous
  * kernel in the stream; x and residual are read, and y written, only after

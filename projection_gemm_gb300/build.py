@@ -22,7 +22,7 @@ OBJ = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libskg.so")
 
-SOURCES = ["skg_api.cu", "skg_gemv.cu", "skg_splitk_tc.cu", "skg_group_tc.cu", "skg_prefetch.cu"]
+SOURCES = ["skg_api.cu", "skg_gemv.cu", "skg_splitk_tc.cu", "skg_group_tc.cu", "skg_prefetch.cu", "skg_rowpar.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

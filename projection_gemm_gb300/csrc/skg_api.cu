@@ -424,6 +424,8 @@ skg_status prepare_splitk_launch(int M, int N, int K, int epi, const void *x, co
     t->epilogue = epi;
     t->timeout_ns = kDefaultTimeoutNs;
     t->pair_reduce = pair_reduce_ok(M, n_tiles, d.split_k, sms);
+    t->chunk_base = 0;
+    t->chunk_count = kChunks;
     *m_pad = d.m_pad;
     *grid = d.grid;
     return SKG_OK;
@@ -447,6 +449,7 @@ struct skg_plan_s {
     unsigned int *err_dev = nullptr;
     cudaStream_t last_stream = nullptr;
     MapCache wmaps, xmaps;
+    int k_rank = 0, k_ranks = 1;      // K shard: canonical chunks [16 r / R, 16 (r + 1) / R)
 };
 
 // A group: several projections of the same M in one persistent launch.
@@ -497,7 +500,7 @@ skg_status ensure_workspace(skg_plan_s *p)
 
 void refresh_prefetch_bytes(skg_plan_s *p)
 {
-    const size_t wbytes = static_cast<size_t>(p->d.N) * p->d.K * 2;
+    const size_t wbytes = static_cast<size_t>(p->d.N) * (p->d.K / p->k_ranks) * 2;   // the W (shard) it runs on
     const double want = p->prefetch_fraction * static_cast<double>(p->l2_bytes);
     p->d.prefetch_bytes = std::min(wbytes, static_cast<size_t>(want)) & ~static_cast<size_t>(15);
 }
@@ -595,6 +598,9 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int t
             return fail(SKG_ERR_UNSUPPORTED, "the tensor-core kernel needs split_k >= 2");
         if (d.kernel_kind == SKG_KERNEL_GEMV && split_k > 8)
             return fail(SKG_ERR_UNSUPPORTED, "the GEMV kernel supports split_k <= 8");
+        if (split_k > kChunks / p->k_ranks)
+            return fail(SKG_ERR_UNSUPPORTED, "split_k=%d exceeds the %d chunks of this plan's K shard", split_k,
+                        kChunks / p->k_ranks);
     }
     const int split = split_k ? split_k : d.split_k;
     const bool gemv_rows = d.kernel_kind == SKG_KERNEL_GEMV && split == 1;
@@ -660,6 +666,8 @@ skg_status skg_plan_force_kernel(skg_plan_t p, int kind)
 {
     if (!p)
         return fail(SKG_ERR_INVALID_ARG, "skg_plan_force_kernel: plan is NULL");
+    if (p->k_ranks > 1 && kind == SKG_KERNEL_GEMV)
+        return fail(SKG_ERR_UNSUPPORTED, "a K-sharded plan runs the split-K kernel");
     skg_plan_desc d;
     skg_status st = query(p->d.M, p->d.N, p->d.K, p->d.epilogue, p->num_sms, p->l2_bytes, &d, kind);
     if (st != SKG_OK)
@@ -676,10 +684,70 @@ skg_status skg_plan_force_kernel(skg_plan_t p, int kind)
             fill_gemv(&d, d.split_k, d.stages, p->num_sms * ctas, p->num_sms);
     }
     p->gemv_ctas_per_sm = ctas;
+    if (p->k_ranks > 1 && d.split_k > kChunks / p->k_ranks)
+        fill_tc(&d, kChunks / p->k_ranks, d.stages, d.tma_burst);
     p->d = d;
     p->wmaps.clear();
     p->xmaps.clear();
     return ensure_workspace(p);
+}
+
+skg_status skg_plan_set_k_shard(skg_plan_t p, int rank, int ranks)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_set_k_shard: plan is NULL");
+    if (ranks != 1 && ranks != 2 && ranks != 4 && ranks != 8)
+        return fail(SKG_ERR_INVALID_ARG, "ranks=%d must be 1, 2, 4 or 8", ranks);
+    if (rank < 0 || rank >= ranks)
+        return fail(SKG_ERR_INVALID_ARG, "rank=%d outside 0..%d", rank, ranks - 1);
+    if (ranks > 1) {
+        if (p->d.epilogue != SKG_EPI_FP32)
+            return fail(SKG_ERR_UNSUPPORTED, "a K shard leaves an fp32 partial: the plan's epilogue must be fp32");
+        if (p->d.K % (kChunks * kBlockK) != 0)
+            return fail(SKG_ERR_UNSUPPORTED, "K=%d: sharding needs K %% %d == 0 (whole, equal canonical chunks)",
+                        p->d.K, kChunks * kBlockK);
+    }
+    skg_plan_desc d = p->d;
+    if (ranks > 1 && d.kernel_kind != SKG_KERNEL_SPLITK_TC) {
+        const skg_status st = query(d.M, d.N, d.K, d.epilogue, p->num_sms, p->l2_bytes, &d, SKG_KERNEL_SPLITK_TC);
+        if (st != SKG_OK)
+            return st;
+        d.pdl = p->d.pdl;
+    }
+    if (d.kernel_kind == SKG_KERNEL_SPLITK_TC && d.split_k > kChunks / ranks)
+        fill_tc(&d, kChunks / ranks, d.stages, d.tma_burst);   // a rank's CTAs split its chunks
+    p->d = d;
+    p->k_rank = rank;
+    p->k_ranks = ranks;
+    refresh_prefetch_bytes(p);
+    p->wmaps.clear();
+    p->xmaps.clear();
+    return ensure_workspace(p);
+}
+
+skg_status skg_combine_partials(int M, int N, int ranks, const float *const *partials, const void *residual,
+                                void *y, int epilogue, void *stream)
+{
+    if (M < 1 || M > 64 || N < 1)
+        return fail(SKG_ERR_INVALID_ARG, "skg_combine_partials: M=%d N=%d", M, N);
+    if (ranks != 1 && ranks != 2 && ranks != 4 && ranks != 8)
+        return fail(SKG_ERR_INVALID_ARG, "skg_combine_partials: ranks=%d must be 1, 2, 4 or 8", ranks);
+    if (!partials || !y)
+        return fail(SKG_ERR_INVALID_ARG, "skg_combine_partials: partials and y must be non-NULL");
+    if (epilogue != SKG_EPI_BF16 && epilogue != SKG_EPI_BF16_RESIDUAL && epilogue != SKG_EPI_FP32)
+        return fail(SKG_ERR_INVALID_ARG, "unknown epilogue %d", epilogue);
+    if ((epilogue == SKG_EPI_BF16_RESIDUAL) != (residual != nullptr))
+        return fail(SKG_ERR_INVALID_ARG, "skg_combine_partials: residual must be given iff the epilogue adds one");
+    for (int r = 0; r < ranks; ++r)
+        if (!partials[r] || !aligned(partials[r], 4))
+            return fail(SKG_ERR_INVALID_ARG, "skg_combine_partials: partial %d is NULL or misaligned", r);
+    if (!aligned(y, epilogue == SKG_EPI_FP32 ? 4 : 2) || (residual && !aligned(residual, 2)))
+        return fail(SKG_ERR_ALIGNMENT, "skg_combine_partials: y / residual miss their element alignment");
+    const cudaError_t e = launch_combine(partials, ranks, static_cast<const uint16_t *>(residual), y, M, N, epilogue,
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "skg_combine_partials launch");
+    return SKG_OK;
 }
 
 skg_status skg_plan_set_pdl(skg_plan_t p, int enable)
@@ -777,10 +845,11 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         e = launch_gemv(g, d.grid, d.pdl != 0, s);
     } else {
         const CUtensorMap *mw = nullptr, *mx = nullptr;
-        skg_status st = p->wmaps.get(W, d.N, d.K, kTileN, &mw);
+        const int k_cols = d.K / p->k_ranks;          // a K shard holds only its chunks' columns
+        skg_status st = p->wmaps.get(W, d.N, k_cols, kTileN, &mw);
         if (st != SKG_OK)
             return st;
-        st = p->xmaps.get(x, d.M, d.K, d.m_pad, &mx);
+        st = p->xmaps.get(x, d.M, k_cols, d.m_pad, &mx);
         if (st != SKG_OK)
             return st;
         const int n_tiles = (d.N + kTileN - 1) / kTileN;
@@ -805,6 +874,8 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         t.epilogue = d.epilogue;
         t.timeout_ns = kDefaultTimeoutNs;
         t.pair_reduce = pair_reduce_ok(d.M, n_tiles, d.split_k, p->num_sms);
+        t.chunk_count = kChunks / p->k_ranks;
+        t.chunk_base = p->k_rank * t.chunk_count;
         e = launch_splitk_tc(*mw, *mx, t, d.m_pad, d.grid, d.pdl != 0, s);
     }
     if (e != cudaSuccess)

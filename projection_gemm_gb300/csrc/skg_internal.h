@@ -76,6 +76,8 @@ struct TcParams {
     int epilogue;
     unsigned long long timeout_ns;
     int pair_reduce;        // 1: the last two arrivals of a tile each reduce half of it
+    int chunk_base;         // first canonical K chunk of this launch (0 unless K is sharded)
+    int chunk_count;        // canonical chunks of this launch (16 unless K is sharded)
 };
 
 // Several projections of the same M in one persistent split-K launch.
@@ -168,6 +170,11 @@ cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, con
 cudaError_t launch_group_tc(const GroupParams &g, int m_pad, int grid, bool pdl, cudaStream_t s);
 int group_ctas_per_sm(int m_pad, int stages);   // co-resident CTAs of the group kernel
 cudaError_t launch_prefetch_l2(const void *base, size_t bytes, cudaStream_t s);
+// y = the R fp32 partials combined in index order by the top levels of the
+// canonical tree (+ residual), one rounding; R in {1, 2, 4, 8}.
+constexpr int kMaxRanks = 8;
+cudaError_t launch_combine(const float *const *partials, int ranks, const uint16_t *res, void *y, int M, int N,
+                           int epilogue, cudaStream_t s);
 cudaError_t launch_debug_wait(unsigned int *err, unsigned long long timeout_ns, cudaStream_t s);
 // Records a failure message for skg_last_error and returns st.
 skg_status set_error(skg_status st, const char *fmt, ...);

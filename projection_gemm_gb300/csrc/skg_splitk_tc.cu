@@ -95,12 +95,16 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x % p.n_tiles;
     const int split = blockIdx.x / p.n_tiles;
-    const int L = kChunks / p.split;
-    const int leaf0 = split * L;
-    const int total_present = chunks_present(p.nkb);
+    // This launch covers canonical chunks [chunk_base, chunk_base +
+    // chunk_count) of K (all 16 unless K is sharded across ranks, when x and
+    // W hold only those chunks' columns): CTA `split` owns an aligned subtree
+    // of L of them.
+    const int L = p.chunk_count / p.split;
+    const int leaf0 = p.chunk_base + split * L;
+    const int total_present = min(chunks_present(p.nkb), p.chunk_base + p.chunk_count);
     const int present = max(0, min(L, total_present - leaf0));
-    const int kb_begin = chunk_begin(leaf0, p.nkb);
-    const int nk = chunk_begin(leaf0 + present, p.nkb) - kb_begin;
+    const int kb_begin = chunk_begin(leaf0, p.nkb) - chunk_begin(p.chunk_base, p.nkb);   // in the shard
+    const int nk = chunk_begin(leaf0 + present, p.nkb) - chunk_begin(leaf0, p.nkb);
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmW);
@@ -335,7 +339,7 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             epi_bar_sync();
             const int role = flags[1];
             if (role) {
-                const int sp = (total_present + L - 1) / L;  // splits holding a value
+                const int sp = (total_present - p.chunk_base + L - 1) / L;  // splits holding a value
                 const int et = threadIdx.x - 64;
                 // outputs of the tile in work items; with pair_reduce the last
                 // arrival takes the second half, the one before it the first

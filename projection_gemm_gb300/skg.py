@@ -27,6 +27,8 @@ SKG_EPI_BF16_RESIDUAL = 1
 SKG_EPI_FP32 = 2
 EPILOGUES = {"bf16": SKG_EPI_BF16, "bf16_residual": SKG_EPI_BF16_RESIDUAL, "fp32": SKG_EPI_FP32}
 
+CANONICAL_CHUNKS = 16     # SKG_CANONICAL_CHUNKS of include/skg.h
+
 SKG_KERNEL_GEMV = 1
 SKG_KERNEL_SPLITK_TC = 2
 KERNEL_NAMES = {SKG_KERNEL_GEMV: "gemv", SKG_KERNEL_SPLITK_TC: "splitk_tc"}
@@ -36,7 +38,7 @@ EXPORTS = (
     "skg_plan_query", "skg_plan", "skg_plan_force", "skg_plan_force_kernel", "skg_plan_set_pdl", "skg_run",
     "skg_prefetch_l2", "skg_plan_set_prefetch_fraction", "skg_plan_info", "skg_plan_check",
     "skg_plan_destroy", "skg_debug_wait_timeout", "skg_last_error", "skg_version",
-    "skg_run_noalloc", "skg_noalloc_check", "skg_plan_set_l2_ahead", "skg_plan_set_next_weight",
+    "skg_run_noalloc", "skg_noalloc_check", "skg_plan_set_k_shard", "skg_combine_partials", "skg_plan_set_l2_ahead", "skg_plan_set_next_weight",
     "skg_group", "skg_group_run", "skg_group_info", "skg_group_check", "skg_group_destroy",
 )
 
@@ -92,6 +94,8 @@ def load(path: str = LIB_PATH):
     lib.skg_debug_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, vp]
     lib.skg_run_noalloc.argtypes = [i, i, i, i, vp, vp, vp, vp, vp]
     lib.skg_noalloc_check.argtypes = [vp]
+    lib.skg_plan_set_k_shard.argtypes = [vp, i, i]
+    lib.skg_combine_partials.argtypes = [i, i, i, P(vp), vp, vp, i, vp]
     lib.skg_plan_set_l2_ahead.argtypes = [vp, i]
     lib.skg_plan_set_next_weight.argtypes = [vp, vp, sz]
     lib.skg_group.argtypes = [i, i, P(i), P(i), P(i), P(i), P(vp)]
@@ -178,6 +182,17 @@ def skg_plan_set_prefetch_fraction(plan: int, fraction: float):
     _check(load().skg_plan_set_prefetch_fraction(plan, float(fraction)))
 
 
+def skg_plan_set_k_shard(plan: int, rank: int, ranks: int):
+    _check(load().skg_plan_set_k_shard(plan, int(rank), int(ranks)))
+
+
+def skg_combine_partials(M: int, N: int, partials, residual, y, epilogue="bf16", stream=None):
+    """partials: R fp32 [M, N] device tensors (or addresses), in rank order."""
+    arr = (ctypes.c_void_p * len(partials))(*[_ptr(t) for t in partials])
+    _check(load().skg_combine_partials(M, N, len(partials), arr, _ptr(residual), _ptr(y), _epi(epilogue),
+                                       _stream(stream)))
+
+
 def skg_plan_info(plan: int) -> dict:
     d = skg_plan_desc()
     _check(load().skg_plan_info(plan, ctypes.byref(d)))
@@ -243,6 +258,9 @@ class Plan:
 
     def set_l2_ahead(self, ahead: int):
         skg_plan_set_l2_ahead(self.handle, ahead)
+
+    def set_k_shard(self, rank: int, ranks: int):
+        skg_plan_set_k_shard(self.handle, rank, ranks)
 
     def run(self, x, W, residual, y, stream=None):
         skg_run(self.handle, x, W, residual, y, stream)
