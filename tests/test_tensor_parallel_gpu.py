@@ -140,5 +140,5 @@ def test_column_parallel_router_and_latent(M, ranks):
         # a row of y depends only on its row of W, and every split gives the
         # same bits: the gathered slices equal the whole launch exactly
         assert np.array_equal(got, out_bits(y_full[i])), f"projection {i}: slices differ from the whole launch"
-        y_ref, s1, _ = O.linear(bits(ts[i].x), bits(ts[i].W))
+        y_ref, s1, _ = O.linear(bits(ts[0].x), bits(ts[i].W))      # both read the same x
         T.check(got, y_ref, s1, K, fp32=e == "fp32", what=f"column-parallel projection {i} x{ranks}")
