@@ -114,6 +114,111 @@ def time_config(M, N, K, epi, cfg, Ws, x, res, y, rounds):
             p.close()
 
 
+def row_config(row):
+    """A table row as the candidate dict time_config takes."""
+    kind, M, N, K, epi, split, stages, grid, aux, ahead = row[:10]
+    cfg = {"split_k": split, "stages": stages, "ahead": ahead}
+    if kind == skg.SKG_KERNEL_SPLITK_TC:
+        cfg["kind"] = kind
+        if aux > 1:
+            cfg["tma_burst"] = aux
+    elif split == 1 and stages >= 2:
+        cfg["tma_burst"] = aux
+    return cfg
+
+
+def sequence_refine(rows, log, steps=150, reps=3, margin_us=0.4, keep=8):
+    """The batch sweep's projections always run as one sequence (M = 1, 2,
+    ..., 64, then again), and a launch's best configuration alone is not
+    always its best next to the others (a neighbour with another shared-memory
+    footprint starts later; look-ahead requests compete with the neighbour's
+    tail).  Coordinate descent over each M's `keep` fastest configurations
+    alone, timing whole eager steps; a change is kept only if it beats the
+    incumbent, timed alternately, by margin_us per step in every one of
+    `reps` pairs.  Returns the rows with the sweep's entries replaced."""
+    N = K = 7168
+    byM = {r[1]: r for r in rows if r[2] == N and r[3] == K and r[4] == skg.EPILOGUES["bf16"]}
+    cands = {}
+    for M in SWEEP_M:
+        seen, c = set(), []
+        for e in sorted((e for e in log if e["N"] == N and e["K"] == K and e["M"] == M), key=lambda e: e["us"]):
+            key = json.dumps(e["config"], sort_keys=True)
+            if key not in seen:
+                seen.add(key)
+                c.append((e["config"], e["us"]))
+        cands[M] = c[:keep]
+    Ws = [generate(Projection(64, N, K, "bf16", seed=900)).W.cuda()]
+    Ws += [Ws[0].roll(i, dims=0).contiguous() for i in range(1, len(SWEEP_M))]
+    xs = {M: generate(Projection(M, N, K, "bf16", seed=901 + M)).x.cuda() for M in SWEEP_M}
+    ys = {M: torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for M in SWEEP_M}
+
+    def plan_for(M, cfg):
+        p = skg.Plan(M, N, K, "bf16")
+        if cfg.get("kind"):
+            p.force_kernel(cfg["kind"])
+        force = {k: v for k, v in cfg.items() if k in ("split_k", "stages", "tma_burst") and v}
+        p.force(**force)
+        p.set_l2_ahead(cfg.get("ahead", 0))
+        return p
+
+    def step_us(plans):
+        for r in range(3):
+            for i, M in enumerate(SWEEP_M):
+                plans[M].run(xs[M], Ws[(i + r) % len(Ws)], None, ys[M])
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for r in range(steps):
+            for i, M in enumerate(SWEEP_M):
+                plans[M].run(xs[M], Ws[(i + r) % len(Ws)], None, ys[M])
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / steps
+
+    choice = {M: row_config(byM[M]) for M in SWEEP_M}
+    us_alone = {M: byM[M][10] for M in SWEEP_M}
+    plans = {M: plan_for(M, choice[M]) for M in SWEEP_M}
+    print(f"sweep step with the table: {step_us(plans):.2f} us", flush=True)
+    for _ in range(2):
+        for M in SWEEP_M:
+            for cfg, us in cands[M]:
+                if cfg == choice[M]:
+                    continue
+                try:
+                    trial = plan_for(M, cfg)
+                except skg.SkgError:
+                    continue
+                incumbent = plans[M]
+                wins = 0
+                for _ in range(reps):
+                    plans[M] = incumbent
+                    t_inc = step_us(plans)
+                    plans[M] = trial
+                    t_new = step_us(plans)
+                    wins += t_new < t_inc - margin_us
+                if wins == reps:
+                    incumbent.close()
+                    choice[M], us_alone[M] = cfg, us
+                    print(f"  M={M}: {cfg} ({t_new:.2f} against {t_inc:.2f} us per step)", flush=True)
+                else:
+                    trial.close()
+                    plans[M] = incumbent
+    print(f"sweep step chosen in sequence: {step_us(plans):.2f} us", flush=True)
+    for p in plans.values():
+        p.close()
+    out = []
+    for r in rows:
+        M = r[1]
+        if r[2] == N and r[3] == K and r[4] == skg.EPILOGUES["bf16"] and M in choice:
+            cfg = choice[M]
+            kind = cfg.get("kind", skg.SKG_KERNEL_GEMV if M <= 2 else skg.SKG_KERNEL_SPLITK_TC)
+            aux = cfg.get("tma_burst", 1)
+            r = (kind, M, N, K, r[4], cfg["split_k"], cfg["stages"], 0, aux, cfg.get("ahead", 0),
+                 us_alone[M], 2 * N * K / us_alone[M] / 1e3)
+        out.append(r)
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out-inc", default=INC)
@@ -121,7 +226,20 @@ def main(argv=None):
     ap.add_argument("--rounds", type=int, default=40)
     ap.add_argument("--only-m", type=int, nargs="*", default=None,
                     help="tune only these M; the table's rows (and the log's entries) for other M are kept")
+    ap.add_argument("--sequence", action="store_true",
+                    help="then refine the batch sweep's rows with the whole sweep step timed (sequence_refine)")
+    ap.add_argument("--sequence-only", action="store_true",
+                    help="only refine the sweep's rows of the existing table in sequence (uses --out-log's "
+                         "timings alone)")
     args = ap.parse_args(argv)
+    if args.sequence_only:
+        build.build()
+        skg.load()
+        torch.cuda.set_device(0)
+        rows = [tuple(r) for r in read_rows(args.out_inc)]
+        log = json.load(open(args.out_log or os.path.join(HERE, "csrc", "skg_plan_tune_log.json")))
+        write_table(args.out_inc, sequence_refine(rows, log), None, 0.0)
+        return
     kept_rows, kept_log = [], []
     if args.only_m:
         kept_rows = [r for r in read_rows(args.out_inc) if r[1] not in args.only_m]
@@ -165,7 +283,15 @@ def main(argv=None):
         torch.cuda.empty_cache()
     rows = sorted(kept_rows + rows, key=lambda r: (r[2], r[3], r[4], r[1]))
     log = kept_log + log
-    with open(args.out_inc, "w") as f:
+    if args.sequence:
+        rows = sequence_refine(rows, log)
+    write_table(args.out_inc, rows, args.out_log and log, time.time() - t0, args.out_log)
+    print(f"wrote {args.out_inc} ({len(rows)} rows)")
+
+
+def write_table(path, rows, log, seconds, log_path=None):
+    """The table rows (and, given log_path, the timing log) as written by main."""
+    with open(path, "w") as f:
         f.write("// skg_plan_table.inc -- measured picker table.\n//\n"
                 "// Each row: { kernel_kind, M, N, K, epilogue, split_k, stages, grid, tma_burst, l2_ahead }.\n"
                 "// stages: TC ring stages / GEMV weight-ring slots per warp (0 = library default);\n"
@@ -174,14 +300,14 @@ def main(argv=None):
                 "// balanced wave (tma_burst = strips per copy for 2 and 3);\n"
                 "// grid = 0 lets the library size the grid.  Written by projection_gemm_gb300/tune.py\n"
                 f"// from back-to-back timings on {torch.cuda.get_device_name(0)} "
-                f"({len(rows)} rows, {time.time() - t0:.0f} s); the comment on each row is the\n"
-                "// measured time per launch and weight-stream rate.\n")
+                f"({len(rows)} rows); the comment on each row is the\n"
+                "// measured time per launch and weight-stream rate (launches of that row alone; the\n"
+                "// batch sweep's rows K = N = 7168 are then chosen with the whole sweep step timed).\n")
         for r in rows:
-            f.write("{%d, %d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.2f us, %.0f GB/s\n" % r)
-    if args.out_log:
-        with open(args.out_log, "w") as f:
+            f.write("{%d, %d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.2f us, %.0f GB/s\n" % tuple(r[:12]))
+    if log_path and log:
+        with open(log_path, "w") as f:
             f.write("[\n" + ",\n".join(json.dumps(r) for r in log) + "\n]\n")
-    print(f"wrote {args.out_inc} ({len(rows)} rows)")
 
 
 if __name__ == "__main__":
