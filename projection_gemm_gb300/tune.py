@@ -127,26 +127,53 @@ def row_config(row):
     return cfg
 
 
-def sequence_refine(rows, log, steps=150, reps=3, margin_us=0.4, keep=8):
+def measured_hbm_gbs():
+    """The measured copy bandwidth of this GPU, else the nominal 8 TB/s."""
+    try:
+        with open(os.path.join(os.path.dirname(HERE), "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"])
+    except Exception:
+        return NOMINAL_HBM_BPS / 1e9
+
+
+def sequence_refine(rows, log, steps=150, reps=3, margin_us=0.4, keep=4, bar_margin=0.02):
     """The batch sweep's projections always run as one sequence (M = 1, 2,
     ..., 64, then again), and a launch's best configuration alone is not
     always its best next to the others (a neighbour with another shared-memory
     footprint starts later; look-ahead requests compete with the neighbour's
-    tail).  Coordinate descent over each M's `keep` fastest configurations
-    alone, timing whole eager steps; a change is kept only if it beats the
-    incumbent, timed alternately, by margin_us per step in every one of
-    `reps` pairs.  Returns the rows with the sweep's entries replaced."""
+    tail).  Coordinate descent over each M's `keep` fastest launch shapes
+    alone (with look-ahead 0 to 4 each), timing whole eager steps; a change is
+    kept only if it beats the incumbent, timed alternately, by margin_us per
+    step in every one of `reps` pairs, and only among launch shapes whose
+    time alone still clears the projection's roofline bar (0.80 at M <= 16,
+    0.70 above) by bar_margin.  Returns the rows with the sweep's entries
+    replaced."""
     N = K = 7168
     byM = {r[1]: r for r in rows if r[2] == N and r[3] == K and r[4] == skg.EPILOGUES["bf16"]}
+    # Candidates: the `keep` fastest launch shapes alone (split, stages, kind,
+    # burst), each with every L2 look-ahead the log holds up to 4 -- in
+    # sequence the next launch's look-ahead requests meet this launch's
+    # latency-bound reduction in L2, which a launch alone does not show.
     cands = {}
     for M in SWEEP_M:
-        seen, c = set(), []
-        for e in sorted((e for e in log if e["N"] == N and e["K"] == K and e["M"] == M), key=lambda e: e["us"]):
-            key = json.dumps(e["config"], sort_keys=True)
-            if key not in seen:
-                seen.add(key)
-                c.append((e["config"], e["us"]))
-        cands[M] = c[:keep]
+        entries = sorted((e for e in log if e["N"] == N and e["K"] == K and e["M"] == M), key=lambda e: e["us"])
+        shapes_, c, seen = [], [], set()
+        for e in entries:
+            shape = json.dumps({k: v for k, v in e["config"].items() if k != "ahead"}, sort_keys=True)
+            if shape not in shapes_:
+                shapes_.append(shape)
+        for shape in shapes_[:keep]:
+            for e in entries:
+                cfg = e["config"]
+                key = json.dumps(cfg, sort_keys=True)
+                if (json.dumps({k: v for k, v in cfg.items() if k != "ahead"}, sort_keys=True) == shape
+                        and cfg.get("ahead", 0) <= 4 and key not in seen):
+                    seen.add(key)
+                    c.append((cfg, e["us"]))
+        # keep a launch that still clears its roofline bar alone, with margin
+        bar = (0.80 if M <= 16 else 0.70) + bar_margin
+        ideal_us = (2 * N * K + 4 * M * K) / (measured_hbm_gbs() * 1e3)
+        cands[M] = [(cfg, us) for cfg, us in c if ideal_us / us >= bar]
     Ws = [generate(Projection(64, N, K, "bf16", seed=900)).W.cuda()]
     Ws += [Ws[0].roll(i, dims=0).contiguous() for i in range(1, len(SWEEP_M))]
     xs = {M: generate(Projection(M, N, K, "bf16", seed=901 + M)).x.cuda() for M in SWEEP_M}
