@@ -136,7 +136,7 @@ def measured_hbm_gbs():
         return NOMINAL_HBM_BPS / 1e9
 
 
-def sequence_refine(rows, log, steps=150, reps=3, margin_us=0.4, keep=4, bar_margin=0.02):
+def sequence_refine(rows, log, steps=150, reps=3, margin_us=0.4, keep=8, bar_margin=0.02):
     """The batch sweep's projections always run as one sequence (M = 1, 2,
     ..., 64, then again), and a launch's best configuration alone is not
     always its best next to the others (a neighbour with another shared-memory
