@@ -120,7 +120,8 @@ typedef struct skg_plan_s *skg_plan_t;
  * [TS]: M <= 2 -> SKG_KERNEL_GEMV, M > 2 -> SKG_KERNEL_SPLITK_TC, except that
  * an M <= 2 shape runs the tensor-core kernel where the table of measured
  * timings holds a tensor-core row for exactly that (M,N,K,epilogue) (written
- * only where it beat every GEMV form on GB300); inside each kind the split
+ * only where it was faster on GB300), or where K is too long for the GEMV
+ * to stage x in shared memory (M = 1: K > 115,200); inside each kind the split
  * and pipeline depth come from that table (nearest M for a listed
  * (N,K,epilogue)), else from an occupancy rule.
  * Constraints: 1 <= M <= 64, N >= 1, K >= 8 and K % 8 == 0, epilogue valid.

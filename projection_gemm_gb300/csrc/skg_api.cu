@@ -210,6 +210,8 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
         kind = force_kind;
     } else if (M <= 2 && table_has_exact(SKG_KERNEL_SPLITK_TC, M, N, K, epi)) {
         kind = SKG_KERNEL_SPLITK_TC;
+    } else if (M <= 2 && gemv_smem_bytes(M, K, 1, 0) > kGemvMaxSmem) {
+        kind = SKG_KERNEL_SPLITK_TC;   // x does not fit the GEMV's shared memory: the split-K kernel streams it
     }
     if (kind == SKG_KERNEL_GEMV && gemv_smem_bytes(M, K, 1, 0) > kGemvMaxSmem)
         return fail(SKG_ERR_UNSUPPORTED, "K=%d too large for the M<=2 kernel (x is staged in shared memory)", K);

@@ -75,7 +75,6 @@ def test_query_shapes(N, K, epi):
     ((4, 128, 12, 0), skg.SKG_ERR_UNSUPPORTED),
     ((4, 128, 0, 0), skg.SKG_ERR_UNSUPPORTED),
     ((4, 128, 128, 3), skg.SKG_ERR_INVALID_ARG),
-    ((1, 128, 200000, 0), skg.SKG_ERR_UNSUPPORTED),
 ])
 def test_query_rejections(args, status):
     with pytest.raises(skg.SkgError) as e:
@@ -144,3 +143,12 @@ def test_plan_table_rows_are_well_formed():
         d = skg.skg_plan_query(M, N, K, epi_name, SMS, L2)
         assert d["kernel"] == ("gemv" if kind == skg.SKG_KERNEL_GEMV else "splitk_tc")
         assert d["split_k"] == split and d["from_table"] == 1
+
+
+def test_long_k_at_small_m_takes_the_split_k_kernel():
+    """x must fit the GEMV's shared memory (M x K x 2 bytes); longer K at
+    M <= 2 is planned on the split-K kernel instead of being rejected."""
+    assert skg.skg_plan_query(1, 4096, 115200, "bf16", SMS, L2)["kernel"] == "gemv"
+    for M, K in ((1, 116736), (1, 1 << 20), (2, 65536)):
+        d = skg.skg_plan_query(M, 4096, K, "bf16", SMS, L2)
+        assert d["kernel"] == "splitk_tc" and d["m_pad"] == 16

@@ -248,6 +248,27 @@ def test_chain_stages_full_size(M):
         _full_size_check(p)
 
 
+@pytest.mark.parametrize("M,N,K,epi,kind", [
+    (64, 32768, 16384, "bf16_residual", "splitk_tc"),   # 1 GiB of weights, the largest M
+    (64, 1, 16384, "bf16", "splitk_tc"),                # a single output row
+    (3, 1, 8, "fp32", "splitk_tc"),                     # the smallest split-K problem
+    (1, 300, 115200, "bf16", "gemv"),                   # the longest K whose x the GEMV stages
+    (1, 512, 131072, "bf16_residual", "splitk_tc"),     # longer K at M = 1: the split-K kernel
+    (2, 700, 65536, "fp32", "splitk_tc"),
+], ids=lambda v: str(v))
+def test_extreme_sizes(M, N, K, epi, kind):
+    """Sizes at the edges of what the kernels take, every output against the
+    oracle; at M <= 2 a K too long for the GEMV's shared-memory x runs the
+    split-K kernel."""
+    case = DeviceCase(Projection(M, N, K, epi, seed=3000 + M + N))
+    try:
+        assert case.plan.info()["kernel"] == kind
+        full_check(case, case.run_bits(), what=f"M={M} N={N} K={K}")
+        case.plan.check()
+    finally:
+        case.close()
+
+
 @pytest.mark.parametrize("M", (1, 2, 8, 64))
 def test_full_size_splits_bit_identical(M):
     case = DeviceCase(sweep(M))
