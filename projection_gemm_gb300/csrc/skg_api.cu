@@ -163,6 +163,19 @@ const TableRow *table_lookup(int kind, int M, int N, int K, int epi)
     return best;
 }
 
+// A GEMV plan with warps sharing rows (split > 1) runs one wave of the CTAs
+// the SMs hold at its ring depth, unless its table row fixes the grid: the
+// host-only query can only estimate that occupancy, the plan measures it.
+bool gemv_grid_from_occupancy(const skg_plan_desc &d)
+{
+    if (d.kernel_kind != SKG_KERNEL_GEMV || d.split_k <= 1)
+        return false;
+    if (!d.from_table)
+        return true;
+    const TableRow *row = table_lookup(SKG_KERNEL_GEMV, d.M, d.N, d.K, d.epilogue);
+    return !row || row->grid <= 0;
+}
+
 bool table_has_exact(int kind, int M, int N, int K, int epi)
 {
     for (const TableRow *r = kTable; r->kind != 0; ++r)
@@ -562,7 +575,7 @@ skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out)
             delete p;
             return fail(SKG_ERR_UNSUPPORTED, "the M<=2 kernel cannot be resident with this shape");
         }
-        if (p->d.split_k > 1 && (!p->d.from_table || p->d.grid <= 0))
+        if (gemv_grid_from_occupancy(p->d))
             fill_gemv(&p->d, p->d.split_k, p->d.stages, sms * p->gemv_ctas_per_sm, sms);
     }
     e = cudaHostAlloc(reinterpret_cast<void **>(&p->err_host), sizeof(unsigned int), cudaHostAllocMapped);
@@ -682,7 +695,7 @@ skg_status skg_plan_force_kernel(skg_plan_t p, int kind)
             return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (ctas < 1)
             return fail(SKG_ERR_UNSUPPORTED, "the M<=2 kernel cannot be resident with this shape");
-        if (d.split_k > 1 && (!d.from_table || d.grid <= 0))
+        if (gemv_grid_from_occupancy(d))
             fill_gemv(&d, d.split_k, d.stages, p->num_sms * ctas, p->num_sms);
     }
     p->gemv_ctas_per_sm = ctas;

@@ -44,6 +44,8 @@ def shapes():
 
 
 def candidates(M, N, K):
+    """Every candidate names its kernel kind: a plan's default kind follows the
+    table being replaced, so a candidate must not depend on it."""
     if M <= 2:
         c = [{"split_k": 1, "stages": 1, "ahead": a} for a in (0, 1, 2)]
         c += [{"split_k": 1, "stages": 2, "tma_burst": b, "ahead": 0} for b in (4, 8)]
@@ -51,6 +53,8 @@ def candidates(M, N, K):
         for split in (2, 4, 8):
             for ring in (2, 3, 4):
                 c.append({"split_k": split, "stages": ring, "ahead": 0})
+        for cfg in c:
+            cfg["kind"] = skg.SKG_KERNEL_GEMV
         # the tensor-core kernel with the tokens padded to 16 columns
         c += [{"kind": skg.SKG_KERNEL_SPLITK_TC, "split_k": sp, "stages": st, "ahead": a}
               for sp in (2, 4, 8) for st in (4, 5, 6) for a in (0, 2)]
@@ -117,9 +121,8 @@ def time_config(M, N, K, epi, cfg, Ws, x, res, y, rounds):
 def row_config(row):
     """A table row as the candidate dict time_config takes."""
     kind, M, N, K, epi, split, stages, grid, aux, ahead = row[:10]
-    cfg = {"split_k": split, "stages": stages, "ahead": ahead}
+    cfg = {"kind": kind, "split_k": split, "stages": stages, "ahead": ahead}
     if kind == skg.SKG_KERNEL_SPLITK_TC:
-        cfg["kind"] = kind
         if aux > 1:
             cfg["tma_burst"] = aux
     elif split == 1 and stages >= 2:
@@ -136,27 +139,34 @@ def measured_hbm_gbs():
         return NOMINAL_HBM_BPS / 1e9
 
 
-def sequence_refine(rows, log, steps=150, reps=3, margin_us=0.4, keep=8, bar_margin=0.02):
-    """The batch sweep's projections always run as one sequence (M = 1, 2,
-    ..., 64, then again), and a launch's best configuration alone is not
-    always its best next to the others (a neighbour with another shared-memory
-    footprint starts later; look-ahead requests compete with the neighbour's
-    tail).  Coordinate descent over each M's `keep` fastest launch shapes
-    alone (with look-ahead 0 to 4 each), timing whole eager steps; a change is
-    kept only if it beats the incumbent, timed alternately, by margin_us per
-    step in every one of `reps` pairs, and only among launch shapes whose
-    time alone still clears the projection's roofline bar (0.80 at M <= 16,
-    0.70 above) by bar_margin.  Returns the rows with the sweep's entries
-    replaced."""
-    N = K = 7168
-    byM = {r[1]: r for r in rows if r[2] == N and r[3] == K and r[4] == skg.EPILOGUES["bf16"]}
-    # Candidates: the `keep` fastest launch shapes alone (split, stages, kind,
-    # burst), each with every L2 look-ahead the log holds up to 4 -- in
-    # sequence the next launch's look-ahead requests meet this launch's
-    # latency-bound reduction in L2, which a launch alone does not show.
+# Projections that always run as one fixed sequence: each workload's step.
+SEQUENCES = {
+    "sweep": lambda: [(M, 7168, 7168, "bf16") for M in SWEEP_M],
+    "chain": lambda: [(M, N, K, epi) for M in CHAIN_M for (K, N, epi) in CHAIN_STAGES],
+}
+
+
+def sequence_refine(rows, log, name="sweep", steps=150, reps=3, margin_us=0.4, keep=8, bar_margin=0.02,
+                    passes=2):
+    """The projections of a workload's step always run as one sequence (the
+    batch sweep M = 1, 2, ..., 64; the decode layer's five stages at M = 1, 8,
+    64), and a launch's best configuration alone is not always its best next
+    to the others: a neighbour with another shared-memory footprint starts
+    later, and the next launch's look-ahead requests meet this launch's
+    latency-bound reduction in L2.  Coordinate descent over each projection's
+    `keep` fastest launch shapes alone (with look-ahead 0 to 4 each), timing
+    whole eager steps; a change is kept only if it beats the incumbent, timed
+    alternately, by margin_us per step in every one of `reps` pairs, and only
+    among launch shapes whose time alone still clears the projection's
+    roofline bar (0.80 at M <= 16, 0.70 above) by bar_margin.  Returns the
+    rows with the sequence's entries replaced."""
+    seq = SEQUENCES[name]()
+    byKey = {(r[1], r[2], r[3], r[4]): r for r in rows}
+    keys = [(M, N, K, skg.EPILOGUES[epi]) for M, N, K, epi in seq]
     cands = {}
-    for M in SWEEP_M:
-        entries = sorted((e for e in log if e["N"] == N and e["K"] == K and e["M"] == M), key=lambda e: e["us"])
+    for (M, N, K, epi) in seq:
+        entries = sorted((e for e in log if (e["M"], e["N"], e["K"], e["epilogue"]) == (M, N, K, epi)
+                          and (M > 2 or "kind" in e["config"])), key=lambda e: e["us"])
         shapes_, c, seen = [], [], set()
         for e in entries:
             shape = json.dumps({k: v for k, v in e["config"].items() if k != "ahead"}, sort_keys=True)
@@ -170,17 +180,20 @@ def sequence_refine(rows, log, steps=150, reps=3, margin_us=0.4, keep=8, bar_mar
                         and cfg.get("ahead", 0) <= 4 and key not in seen):
                     seen.add(key)
                     c.append((cfg, e["us"]))
-        # keep a launch that still clears its roofline bar alone, with margin
         bar = (0.80 if M <= 16 else 0.70) + bar_margin
-        ideal_us = (2 * N * K + 4 * M * K) / (measured_hbm_gbs() * 1e3)
-        cands[M] = [(cfg, us) for cfg, us in c if ideal_us / us >= bar]
-    Ws = [generate(Projection(64, N, K, "bf16", seed=900)).W.cuda()]
-    Ws += [Ws[0].roll(i, dims=0).contiguous() for i in range(1, len(SWEEP_M))]
-    xs = {M: generate(Projection(M, N, K, "bf16", seed=901 + M)).x.cuda() for M in SWEEP_M}
-    ys = {M: torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for M in SWEEP_M}
+        p = Projection(M, N, K, epi)
+        ideal_us = p.algorithmic_bytes() / (measured_hbm_gbs() * 1e3)
+        cands[(M, N, K, skg.EPILOGUES[epi])] = [(cfg, us) for cfg, us in c if ideal_us / us >= bar]
+    ops = []
+    for i, (M, N, K, epi) in enumerate(seq):
+        t = generate(Projection(M, N, K, epi, seed=950 + i))
+        ops.append(dict(W=t.W.cuda(), x=t.x.cuda(), res=None if t.res is None else t.res.cuda(),
+                        y=torch.empty(M, N, dtype=torch.float32 if epi == "fp32" else torch.bfloat16,
+                                      device="cuda")))
 
-    def plan_for(M, cfg):
-        p = skg.Plan(M, N, K, "bf16")
+    def plan_for(key, cfg):
+        M, N, K, epi = key
+        p = skg.Plan(M, N, K, epi)
         if cfg.get("kind"):
             p.force_kernel(cfg["kind"])
         force = {k: v for k, v in cfg.items() if k in ("split_k", "stages", "tma_burst") and v}
@@ -189,59 +202,61 @@ def sequence_refine(rows, log, steps=150, reps=3, margin_us=0.4, keep=8, bar_mar
         return p
 
     def step_us(plans):
-        for r in range(3):
-            for i, M in enumerate(SWEEP_M):
-                plans[M].run(xs[M], Ws[(i + r) % len(Ws)], None, ys[M])
+        def one():
+            for key, o in zip(keys, ops):
+                plans[key].run(o["x"], o["W"], o["res"], o["y"])
+        for _ in range(3):
+            one()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        for r in range(steps):
-            for i, M in enumerate(SWEEP_M):
-                plans[M].run(xs[M], Ws[(i + r) % len(Ws)], None, ys[M])
+        for _ in range(steps):
+            one()
         b.record()
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e3 / steps
 
-    choice = {M: row_config(byM[M]) for M in SWEEP_M}
-    us_alone = {M: byM[M][10] for M in SWEEP_M}
-    plans = {M: plan_for(M, choice[M]) for M in SWEEP_M}
-    print(f"sweep step with the table: {step_us(plans):.2f} us", flush=True)
-    for _ in range(2):
-        for M in SWEEP_M:
-            for cfg, us in cands[M]:
-                if cfg == choice[M]:
+    choice = {k: row_config(byKey[k]) for k in keys}
+    us_alone = {k: byKey[k][10] for k in keys}
+    plans = {k: plan_for(k, choice[k]) for k in keys}
+    print(f"{name} step with the table: {step_us(plans):.2f} us", flush=True)
+    for _ in range(passes):
+        for key in keys:
+            for cfg, us in cands[key]:
+                if cfg == choice[key]:
                     continue
                 try:
-                    trial = plan_for(M, cfg)
+                    trial = plan_for(key, cfg)
                 except skg.SkgError:
                     continue
-                incumbent = plans[M]
+                incumbent = plans[key]
                 wins = 0
                 for _ in range(reps):
-                    plans[M] = incumbent
+                    plans[key] = incumbent
                     t_inc = step_us(plans)
-                    plans[M] = trial
+                    plans[key] = trial
                     t_new = step_us(plans)
                     wins += t_new < t_inc - margin_us
                 if wins == reps:
                     incumbent.close()
-                    choice[M], us_alone[M] = cfg, us
-                    print(f"  M={M}: {cfg} ({t_new:.2f} against {t_inc:.2f} us per step)", flush=True)
+                    choice[key], us_alone[key] = cfg, us
+                    print(f"  {key}: {cfg} ({t_new:.2f} against {t_inc:.2f} us per step)", flush=True)
                 else:
                     trial.close()
-                    plans[M] = incumbent
-    print(f"sweep step chosen in sequence: {step_us(plans):.2f} us", flush=True)
+                    plans[key] = incumbent
+    print(f"{name} step chosen in sequence: {step_us(plans):.2f} us", flush=True)
     for p in plans.values():
         p.close()
     out = []
     for r in rows:
-        M = r[1]
-        if r[2] == N and r[3] == K and r[4] == skg.EPILOGUES["bf16"] and M in choice:
-            cfg = choice[M]
+        key = (r[1], r[2], r[3], r[4])
+        if key in choice:
+            cfg = choice[key]
+            M, N, K = key[:3]
             kind = cfg.get("kind", skg.SKG_KERNEL_GEMV if M <= 2 else skg.SKG_KERNEL_SPLITK_TC)
             aux = cfg.get("tma_burst", 1)
             r = (kind, M, N, K, r[4], cfg["split_k"], cfg["stages"], 0, aux, cfg.get("ahead", 0),
-                 us_alone[M], 2 * N * K / us_alone[M] / 1e3)
+                 us_alone[key], 2 * N * K / us_alone[key] / 1e3)
         out.append(r)
     return out
 
@@ -253,10 +268,10 @@ def main(argv=None):
     ap.add_argument("--rounds", type=int, default=40)
     ap.add_argument("--only-m", type=int, nargs="*", default=None,
                     help="tune only these M; the table's rows (and the log's entries) for other M are kept")
-    ap.add_argument("--sequence", action="store_true",
-                    help="then refine the batch sweep's rows with the whole sweep step timed (sequence_refine)")
-    ap.add_argument("--sequence-only", action="store_true",
-                    help="only refine the sweep's rows of the existing table in sequence (uses --out-log's "
+    ap.add_argument("--sequence", nargs="*", choices=sorted(SEQUENCES), default=None,
+                    help="then refine these workloads' rows with their whole step timed (sequence_refine)")
+    ap.add_argument("--sequence-only", nargs="+", choices=sorted(SEQUENCES), default=None,
+                    help="only refine these workloads' rows of the existing table in sequence (uses --out-log's "
                          "timings alone)")
     args = ap.parse_args(argv)
     if args.sequence_only:
@@ -265,7 +280,9 @@ def main(argv=None):
         torch.cuda.set_device(0)
         rows = [tuple(r) for r in read_rows(args.out_inc)]
         log = json.load(open(args.out_log or os.path.join(HERE, "csrc", "skg_plan_tune_log.json")))
-        write_table(args.out_inc, sequence_refine(rows, log), None, 0.0)
+        for name in args.sequence_only:
+            rows = sequence_refine(rows, log, name)
+        write_table(args.out_inc, rows, None, 0.0)
         return
     kept_rows, kept_log = [], []
     if args.only_m:
@@ -310,8 +327,8 @@ def main(argv=None):
         torch.cuda.empty_cache()
     rows = sorted(kept_rows + rows, key=lambda r: (r[2], r[3], r[4], r[1]))
     log = kept_log + log
-    if args.sequence:
-        rows = sequence_refine(rows, log)
+    for name in (args.sequence or []):
+        rows = sequence_refine(rows, log, name)
     write_table(args.out_inc, rows, args.out_log and log, time.time() - t0, args.out_log)
     print(f"wrote {args.out_inc} ({len(rows)} rows)")
 
@@ -328,8 +345,9 @@ def write_table(path, rows, log, seconds, log_path=None):
                 "// grid = 0 lets the library size the grid.  Written by projection_gemm_gb300/tune.py\n"
                 f"// from back-to-back timings on {torch.cuda.get_device_name(0)} "
                 f"({len(rows)} rows); the comment on each row is the\n"
-                "// measured time per launch and weight-stream rate (launches of that row alone; the\n"
-                "// batch sweep's rows K = N = 7168 are then chosen with the whole sweep step timed).\n")
+                "// measured time per launch and weight-stream rate (launches of that row alone; the rows\n"
+                "// of the batch sweep and the decode-layer chain are then chosen with their whole step\n"
+                "// timed).\n")
         for r in rows:
             f.write("{%d, %d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.2f us, %.0f GB/s\n" % tuple(r[:12]))
     if log_path and log:

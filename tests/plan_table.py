@@ -1,7 +1,8 @@
 """The kernel kind the picker should choose, read from the compiled-in table.
 
 M <= 2 runs the GEMV unless the measured table holds a tensor-core row for
-exactly that (M, N, K, epilogue); M > 2 always runs the tensor-core kernel.
+exactly that (M, N, K, epilogue) or x (M x K bf16) does not fit the GEMV's
+226 KB of shared memory; M > 2 always runs the tensor-core kernel.
 """
 from __future__ import annotations
 
@@ -13,21 +14,20 @@ _INC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 _EPI = {"bf16": 0, "bf16_residual": 1, "fp32": 2}
 
 
-def _tc_rows():
-    rows = set()
+def table_rows():
+    """Every row of the table: (kind, M, N, K, epilogue, split, stages, grid, aux, ahead)."""
+    rows = []
     for line in open(_INC):
         m = re.match(r"^\{([-\d, ]+)\}", line)
         if m:
-            v = [int(a) for a in m.group(1).split(",")]
-            if v[0] == 2:
-                rows.add((v[1], v[2], v[3], v[4]))
+            rows.append(tuple(int(a) for a in m.group(1).split(",")))
     return rows
 
 
-_TC = _tc_rows()
+_TC = {(r[1], r[2], r[3], r[4]) for r in table_rows() if r[0] == 2}
 
 
 def expected_kind(M: int, N: int, K: int, epilogue: str) -> str:
-    if M > 2 or (M, N, K, _EPI[epilogue]) in _TC:
+    if M > 2 or (M, N, K, _EPI[epilogue]) in _TC or M * K * 2 > 226 * 1024:
         return "splitk_tc"
     return "gemv"

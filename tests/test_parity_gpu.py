@@ -325,3 +325,24 @@ def test_force_kernel_rejections_keep_the_plan():
         case.plan.check()
     finally:
         case.close()
+
+
+def test_table_rows_launch_what_the_tuner_measured():
+    """A measured GEMV row whose warps share rows (split > 1) leaves the grid
+    to the library: the plan must launch the grid the tuner timed, one wave
+    at that ring depth's occupancy -- the same as forcing the row's split and
+    ring."""
+    from tests.plan_table import table_rows
+    rows = [r for r in table_rows() if r[0] == skg.SKG_KERNEL_GEMV and r[5] > 1 and r[7] == 0]
+    assert rows, "no GEMV row with warps sharing rows to check"
+    for kind, M, N, K, epi, split, stages, grid, aux, ahead in rows:
+        a = skg.Plan(M, N, K, epi)
+        b = skg.Plan(M, N, K, epi)
+        try:
+            b.force(split_k=split, stages=stages)
+            ia, ib = a.info(), b.info()
+            assert ia["from_table"] == 1 and (ia["split_k"], ia["stages"]) == (split, stages)
+            assert ia["grid"] == ib["grid"], (M, N, K, ia["grid"], ib["grid"])
+        finally:
+            a.close()
+            b.close()
