@@ -682,7 +682,67 @@ def chain_variants(wl, s, torch_stream, steps, l2_bytes):
     set_next(0.0)
     wl.bind_streams([torch_stream])
     out["group_launch_per_m_ordered"] = chain_groups(wl, s, torch_stream, steps)
+    out["router_and_latent_as_one_launch"] = chain_router_latent(wl, s, torch_stream, steps)
     return out
+
+
+def chain_router_latent(wl, s, torch_stream, steps):
+    """The chain with its router-score GEMM and latent input projection,
+    which read the same hidden state, as one group launch without ordering
+    (the single-GPU form of the pages' router + latent projection as one
+    GEMM); the other three projections as their own launches.  Both read the
+    router stage's x here."""
+    import torch
+    from projection_gemm_gb300 import inputs as I
+    from projection_gemm_gb300 import skg
+    per_m = len(I.CHAIN_STAGES)
+    pairs = []
+    try:
+        for j, m in enumerate(I.CHAIN_M):
+            r, l = wl.ops[j * per_m + 2], wl.ops[j * per_m + 3]
+            g = skg.Group(m, [r["p"].N, l["p"].N], [r["p"].K, l["p"].K], [r["p"].epilogue, l["p"].epilogue], None)
+            pairs.append((g, [r["args"][0]] * 2, [r["args"][1], l["args"][1]], [r["args"][3], l["args"][3]]))
+
+        def step(events=None):
+            for j in range(len(I.CHAIN_M)):
+                if events is not None:
+                    events[j].record(torch_stream)
+                base = j * per_m
+                for i in (0, 1):
+                    wl.launch(wl.ops[base + i], s)
+                g, xs, ws, ys = pairs[j]
+                skg.skg_group_run(g.handle, xs, ws, None, ys, s)
+                wl.launch(wl.ops[base + 4], s)
+            if events is not None:
+                events[-1].record(torch_stream)
+        for _ in range(3):
+            step()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(torch_stream)
+        for _ in range(steps):
+            step()
+        b.record(torch_stream)
+        torch.cuda.synchronize()
+        el = a.elapsed_time(b) / 1e3
+        seg_us = [[] for _ in I.CHAIN_M]
+        for _ in range(12):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(I.CHAIN_M) + 1)]
+            step(ev)
+            torch.cuda.synchronize()
+            for j in range(len(I.CHAIN_M)):
+                seg_us[j].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+        res = {"us_per_step": round(el / steps * 1e6, 3), "gbs": round(wl.weight_bytes() * steps / el / 1e9, 1),
+               "per_m": {}}
+        for j, m in enumerate(I.CHAIN_M):
+            us = statistics.median(seg_us[j])
+            wb = sum(o["p"].weight_bytes() for o in wl.ops[j * per_m:(j + 1) * per_m])
+            res["per_m"][f"m{m}"] = {"us": round(us, 3), "weight_gbs": round(wb / us / 1e3, 1)}
+        for g, *_ in pairs:
+            g.check()
+        return res
+    finally:
+        for g, *_ in pairs:
+            g.close()
 
 
 def chain_groups(wl, s, torch_stream, steps):
