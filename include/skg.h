@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define SKG_VERSION 2
+#define SKG_VERSION 3
 
 /* Symbols of the ABI are exported; everything else in the library is hidden. */
 #if defined(__GNUC__)
@@ -110,6 +110,12 @@ typedef struct skg_plan_desc {
     int l2_ahead;           /* weights requested into L2 ahead of use: TC k-blocks after the
                                ring, before the wait for the previous kernel; GEMV (split 1)
                                batches of the row; 0 = none */
+    int reducers;           /* TC: the last `reducers` CTAs to finish a tile share its final
+                               reduction (1, 2, 4 or 8; a launch uses fewer where the split is
+                               smaller or the waiting CTAs could fill the SMs); GEMV: 0 */
+    int ctas_per_sm;        /* CTAs one SM holds at once: TC, the CUDA occupancy calculator for
+                               this launch shape; GEMV, the count the plan sizes one-wave grids
+                               from.  Filled by skg_plan_info; 0 from skg_plan_query */
 } skg_plan_desc;
 
 typedef struct skg_plan_s *skg_plan_t;
@@ -251,6 +257,20 @@ SKG_API skg_status skg_prefetch_l2(skg_plan_t next, const void *W_next, void *si
  * whole-row bulk-copy form (stages 2) ignore it.
  */
 SKG_API skg_status skg_plan_set_l2_ahead(skg_plan_t plan, int ahead);
+
+/*
+ * skg_plan_set_reducers -- [TS] the split-K kernel's final reduction of a
+ * 128-row tile (its S partial sums combined by the top levels of the
+ * canonical tree, the residual added, one rounding) is done by the last R
+ * CTAs of the tile to finish, each taking 1/R of the tile's outputs; all but
+ * the last wait, with the plan's bounded wait, for the others.  R = 1, 2, 4
+ * or 8.  The output bits do not depend on R.  A launch uses min(R, split_k)
+ * (1 at split 16), halved until tiles x (R - 1) waiting CTAs are fewer than
+ * the CTAs the SMs hold at once; the plan's description reports that count
+ * for its current launch shape.  Errors: SKG_ERR_INVALID_ARG (R),
+ * SKG_ERR_UNSUPPORTED (a GEMV plan), SKG_ERR_CUDA.
+ */
+SKG_API skg_status skg_plan_set_reducers(skg_plan_t plan, int reducers);
 
 /*
  * skg_plan_set_next_weight -- [PF] inside the launch instead of on a side

@@ -44,12 +44,12 @@ skg_status cuda_fail(cudaError_t e, const char *what)
 
 // ------------------------------------------------------------ picker table
 struct TableRow {
-    int kind, M, N, K, epi, split, stages, grid, burst, ahead;
+    int kind, M, N, K, epi, split, stages, grid, burst, ahead, reducers;
 };
 
 const TableRow kTable[] = {
 #include "skg_plan_table.inc"
-    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0}  // sentinel
+    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0}  // sentinel
 };
 
 bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
@@ -263,11 +263,17 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
     } else {
         int split, stages = 0, burst = 1;
         const int n_tiles = (N + kTileN - 1) / kTileN;
+        // measured default: at M > 16 the partials take a lone reducer two
+        // rounds of loads, and two reducers per tile save 1 to 2 us a launch
+        // at M = 64; at M <= 16 the wait costs more than it saves
+        d->reducers = M > 16 ? 2 : 1;
         if (row) {
             split = row->split;
             stages = row->stages;
             burst = row->burst;
             d->l2_ahead = row->ahead;
+            if (row->reducers > 0)
+                d->reducers = row->reducers;
             d->from_table = 1;
         } else {
             // Measured on GB300 (back-to-back launches): about 1.5 CTAs per
@@ -356,16 +362,19 @@ struct MapCache {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// The last two arrivals of a tile share its reduction at M > 16, where the
-// partials take a last CTA two rounds of loads (measured on GB300: 1 to 2 us
-// saved per launch at M = 64; at M <= 16 the wait costs more than it saves).
-// Safe only when at most one CTA per tile waits and the waiters cannot fill
-// the SMs: every other CTA of the grid runs to completion without waiting,
-// so the CTA a waiter waits for always gets an SM.  Splits of 16 reduce in
-// one CTA (per-row form).
-int pair_reduce_ok(int M, int n_tiles, int split, int num_sms)
+// The reducers per tile a launch may use: at most the plan's R, the split
+// (splits of 16 reduce in one CTA), and few enough that the waiting CTAs,
+// tiles x (R - 1), stay fewer than the CTAs the SMs hold at once
+// (`slots`): every other CTA runs to completion without waiting, so the
+// CTAs a waiter waits for always get an SM.
+int safe_reducers(int want, int n_tiles, int split, int slots)
 {
-    return (M > 16 && split <= 8 && n_tiles < num_sms) ? 1 : 0;
+    if (split > 8)
+        return 1;
+    int r = std::max(1, std::min(want, split));
+    while (r > 1 && static_cast<long long>(n_tiles) * (r - 1) >= slots)
+        r /= 2;
+    return r;
 }
 
 } // namespace
@@ -438,7 +447,11 @@ skg_status prepare_splitk_launch(int M, int N, int K, int epi, const void *x, co
     t->ahead = d.l2_ahead;
     t->epilogue = epi;
     t->timeout_ns = kDefaultTimeoutNs;
-    t->pair_reduce = pair_reduce_ok(M, n_tiles, d.split_k, sms);
+    int occ = 1;
+    e = tc_occupancy(d.m_pad, d.stages, &occ);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    t->reducers = safe_reducers(d.reducers, n_tiles, d.split_k, sms * std::max(1, occ));
     t->chunk_base = 0;
     t->chunk_count = kChunks;
     *m_pad = d.m_pad;
@@ -457,6 +470,8 @@ struct skg_plan_s {
     void *ws = nullptr;               // [S][tiles][M][128] fp32 partials, then counters
     size_t ws_cap = 0;
     std::vector<void *> retired;      // outgrown workspaces: a captured graph may still use them
+    int occ_m_pad = 0, occ_stages = 0; // shape of the split-K launch tc_ctas_per_sm was measured for
+    int tc_ctas_per_sm = 1;
     const void *next_w = nullptr;     // prefetched into L2 by this plan's launches
     size_t next_bytes = 0;
     int gemv_ctas_per_sm = 0;         // measured occupancy of the GEMV kernel
@@ -794,6 +809,25 @@ skg_status skg_plan_set_l2_ahead(skg_plan_t p, int ahead)
     return SKG_OK;
 }
 
+skg_status skg_plan_set_reducers(skg_plan_t p, int reducers)
+{
+    if (!p)
+        return fail(SKG_ERR_INVALID_ARG, "skg_plan_set_reducers: plan is NULL");
+    if (reducers != 1 && reducers != 2 && reducers != 4 && reducers != 8)
+        return fail(SKG_ERR_INVALID_ARG, "reducers=%d must be 1, 2, 4 or 8", reducers);
+    if (p->d.kernel_kind != SKG_KERNEL_SPLITK_TC)
+        return fail(SKG_ERR_UNSUPPORTED, "reducers apply to the split-K kernel only");
+    // the count a launch of the current shape uses (skg_run applies the same
+    // bound again after any later change of the shape)
+    int occ = 1;
+    const cudaError_t e = tc_occupancy(p->d.m_pad, p->d.stages, &occ);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    const int n_tiles = (p->d.N + kTileN - 1) / kTileN;
+    p->d.reducers = safe_reducers(reducers, n_tiles, p->d.split_k, p->num_sms * std::max(1, occ));
+    return SKG_OK;
+}
+
 skg_status skg_plan_set_prefetch_fraction(skg_plan_t p, double fraction)
 {
     if (!p)
@@ -810,6 +844,13 @@ skg_status skg_plan_info(skg_plan_t p, skg_plan_desc *out)
     if (!p || !out)
         return fail(SKG_ERR_INVALID_ARG, "skg_plan_info: NULL argument");
     *out = p->d;
+    int occ = p->gemv_ctas_per_sm;
+    if (p->d.kernel_kind == SKG_KERNEL_SPLITK_TC) {
+        const cudaError_t e = tc_occupancy(p->d.m_pad, p->d.stages, &occ);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    }
+    out->ctas_per_sm = occ;
     return SKG_OK;
 }
 
@@ -888,7 +929,16 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         t.next_bytes = p->next_bytes;
         t.epilogue = d.epilogue;
         t.timeout_ns = kDefaultTimeoutNs;
-        t.pair_reduce = pair_reduce_ok(d.M, n_tiles, d.split_k, p->num_sms);
+        if (p->occ_m_pad != d.m_pad || p->occ_stages != d.stages) {
+            int occ = 1;
+            e = tc_occupancy(d.m_pad, d.stages, &occ);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+            p->occ_m_pad = d.m_pad;
+            p->occ_stages = d.stages;
+            p->tc_ctas_per_sm = std::max(1, occ);
+        }
+        t.reducers = safe_reducers(d.reducers, n_tiles, d.split_k, p->num_sms * p->tc_ctas_per_sm);
         t.chunk_count = kChunks / p->k_ranks;
         t.chunk_base = p->k_rank * t.chunk_count;
         e = launch_splitk_tc(*mw, *mx, t, d.m_pad, d.grid, d.pdl != 0, s);

@@ -16,6 +16,7 @@ constexpr int kChunks = SKG_CANONICAL_CHUNKS;  // leaves of the canonical tree
 constexpr int kTileN = 128;                    // W rows per tcgen05 tile (MMA M)
 constexpr int kBlockK = 64;                    // k per TMA box: 64 bf16 = 128 B
 constexpr int kTcThreads = 320;                // producer, MMA, 8 epilogue warps
+constexpr int kTmemColsPerSm = 512;           // tensor memory: 128 lanes x 512 fp32 columns per SM
 constexpr int kGemvThreads = 256;              // 8 warps
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s bounded waits
@@ -75,7 +76,7 @@ struct TcParams {
     size_t next_bytes;      // bytes of next_w the grid asks the L2 for (multiple of 16)
     int epilogue;
     unsigned long long timeout_ns;
-    int pair_reduce;        // 1: the last two arrivals of a tile each reduce half of it
+    int reducers;           // R: the last R arrivals of a tile each reduce 1/R of it (1, 2, 4, 8)
     int chunk_base;         // first canonical K chunk of this launch (0 unless K is sharded)
     int chunk_count;        // canonical chunks of this launch (16 unless K is sharded)
 };
@@ -159,6 +160,7 @@ int gemv_span_grid(int M, int N, int K, int batch_strips, int num_sms);
 constexpr int kGemvMaxSmem = 226 * 1024;      // x (M * K * 2 bytes) + the weight rings (static smem needs the rest)
 int tc_max_stages(int m_pad, int smem_limit);
 int tc_tmem_cols(int m_pad);                  // TMEM columns one CTA allocates
+cudaError_t tc_occupancy(int m_pad, int stages, int *ctas_per_sm);  // split-K CTAs one SM holds
 constexpr int kTcDefaultStages = 4;
 
 // Launchers (return the cudaError_t of the launch).

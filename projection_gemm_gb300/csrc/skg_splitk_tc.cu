@@ -22,9 +22,10 @@
 // sums are combined by one balanced binary tree (empty chunks skipped).  The
 // S CTAs of a tile each own an aligned subtree of 16/S chunks and write its
 // value to the plan's fp32 workspace; the last CTA to arrive (an atomic
-// counter picks it; no CTA ever waits for another) combines the S values by
-// the top levels of the same tree, in index order, adds the residual in
-// fp32, rounds once to bf16 and writes y.  Every allowed S gives the same
+// counter picks it) combines the S values by the top levels of the same
+// tree, in index order, adds the residual in fp32, rounds once to bf16 and
+// writes y.  With R > 1 reducers per tile, the last R arrivals each wait
+// for the others and combine a 1/R share of the tile's outputs the same way.  Every allowed S gives the same
 // bits, and the arrival order never changes them.
 //
 // Ordering rule of the pages (background 2, the activation read hoisted above
@@ -37,6 +38,7 @@
 // own asynchronous copies / MMAs, and the CTA frees its TMEM and returns.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "skg_internal.h"
@@ -47,11 +49,13 @@ namespace {
 
 #include "skg_tc_common.cuh"
 
-// Second-to-last arrival of a tile: poll the tile's counter (acquire, GPU
-// scope) until all `target` arrivals are in, for at most timeout_ns, or until
-// another role of the CTA gave up.  The CTA it waits for belongs to the same
-// grid and never waits itself, and at most one CTA per tile waits, so the
-// host enables this only while the tiles are fewer than the SMs.
+// A reducer that is not the tile's last arrival: poll the tile's counter
+// (acquire, GPU scope) until all `target` arrivals are in, for at most
+// timeout_ns, or until another role of the CTA gave up.  Every CTA arrives
+// before it waits, so a waiter waits only for CTAs that never wait; the host
+// allows R reducers per tile only while the waiters, tiles x (R - 1), are
+// fewer than the CTAs the SMs hold at once, so a CTA waited for always finds
+// a free slot.
 __device__ __forceinline__ bool wait_arrivals(const unsigned *ctr, unsigned target, uint64_t timeout_ns,
                                               volatile int *abort)
 {
@@ -310,26 +314,27 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             // scope; the last arriver's acquire, passed on by the next
             // barrier, orders its reads of all partials after the stores.
             epi_bar_sync();
-            const bool pair = p.pair_reduce && p.split <= 8;
+            // The last R arrivals of the tile share its reduction: each waits
+            // (bounded) until every arrival is in, then reduces its share of
+            // the tile's outputs.  Splits of 16 reduce in one CTA.
+            const int R = p.split <= 8 ? max(1, min(p.reducers, p.split)) : 1;
             if (ew == 0 && lane == 0) {
                 // Low 16 bits of the tile's counter: arrivals; high bits:
                 // reducers that have seen every arrival.
-                const unsigned old = atom_add_acq_rel_gpu(&p.counters[tile], 1u) & 0xFFFFu;
-                int role = 0;
-                if (old == static_cast<unsigned>(p.split - 1)) {
-                    role = 1;                    // last arrival
-                } else if (pair && old == static_cast<unsigned>(p.split - 2)) {
-                    // second to last: wait (bounded) for the last arrival,
-                    // then reduce the first half of the tile's outputs
-                    if (wait_arrivals(&p.counters[tile], static_cast<unsigned>(p.split), p.timeout_ns, &flags[0]))
-                        role = 2;
+                const int old = static_cast<int>(atom_add_acq_rel_gpu(&p.counters[tile], 1u) & 0xFFFFu);
+                const int first = p.split - R;
+                int role = 0;   // 1 + this CTA's share of the reduction; 0: none
+                if (old >= first) {
+                    if (old == p.split - 1 ||
+                        wait_arrivals(&p.counters[tile], static_cast<unsigned>(p.split), p.timeout_ns, &flags[0]))
+                        role = old - first + 1;
                     else
                         record_failure(p, &flags[0], kErrTimeoutEpilogue);
                 }
-                if (role && pair) {
-                    // the second reducer to get here has seen both see every
-                    // arrival: it returns the counter to zero
-                    if ((atom_add_acq_rel_gpu(&p.counters[tile], 1u << 16) >> 16) == 1)
+                if (role && R > 1) {
+                    // the last reducer to see every arrival returns the
+                    // counter to zero: no one polls it any more
+                    if ((atom_add_acq_rel_gpu(&p.counters[tile], 1u << 16) >> 16) == static_cast<unsigned>(R - 1))
                         p.counters[tile] = 0;
                 } else if (role) {
                     p.counters[tile] = 0;
@@ -341,12 +346,12 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             if (role) {
                 const int sp = (total_present - p.chunk_base + L - 1) / L;  // splits holding a value
                 const int et = threadIdx.x - 64;
-                // outputs of the tile in work items; with pair_reduce the last
-                // arrival takes the second half, the one before it the first
+                // work items: 4 rows of one column m; share r of R takes
+                // whole columns [r * ceil(M / R), (r + 1) * ceil(M / R))
                 const int items = p.M * (kTileN / 4);
-                const int mid = pair ? (items / 2 + 31) / 32 * 32 : 0;
-                const int i0 = role == 2 ? 0 : mid;
-                const int i1 = role == 2 ? mid : items;
+                const int share = (p.M + R - 1) / R * (kTileN / 4);
+                const int i0 = min(items, (role - 1) * share);
+                const int i1 = min(items, role * share);
                 constexpr int kL = MPAD <= 32 ? 8 : 16;   // 16-byte loads in flight per thread
                 switch (p.split) {
                 case 2: reduce_tile_v4<2, kL>(p, tile, sp, et, i0, i1); break;
@@ -373,11 +378,11 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     }
 }
 
+// The kernel's shared-memory attributes, set once per device before its
+// first launch or occupancy query.
 template <int MPAD>
-cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p, int grid,
-                      bool pdl, cudaStream_t s)
+cudaError_t set_tc_attrs()
 {
-    const int smem = tc_smem_bytes(MPAD, p.stages);
     static int attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -385,7 +390,7 @@ cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcPa
         return e;
     if (dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
-    if (__atomic_load_n(&attr_set[dev], __ATOMIC_ACQUIRE) < smem) {
+    if (__atomic_load_n(&attr_set[dev], __ATOMIC_ACQUIRE) == 0) {
         e = cudaFuncSetAttribute(splitk_tc_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
         if (e != cudaSuccess)
             return e;
@@ -393,8 +398,61 @@ cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcPa
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
-        __atomic_store_n(&attr_set[dev], 232448, __ATOMIC_RELEASE);
+        __atomic_store_n(&attr_set[dev], 1, __ATOMIC_RELEASE);
     }
+    return cudaSuccess;
+}
+
+// CTAs of one launch shape an SM holds at once, from the kernel's
+// registers, shared memory, threads and TMEM columns.  Measured on GB300:
+// cudaOccupancyMaxActiveBlocksPerMultiprocessor answers 1 for this kernel at
+// every shape, while the profiler's launch statistics show 2 CTAs per SM at
+// m_pad 64 (register and shared-memory limits both 2), so the limits are
+// taken here one by one.
+template <int MPAD>
+cudaError_t occupancy_tc(int stages, int *ctas_per_sm)
+{
+    cudaError_t e = set_tc_attrs<MPAD>();
+    if (e != cudaSuccess)
+        return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, splitk_tc_kernel<MPAD>);
+    if (e != cudaSuccess)
+        return e;
+    int dev = 0, regs_sm = 0, smem_sm = 0, smem_rsv = 0, threads_sm = 0, blocks_sm = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&blocks_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev);
+    if (e != cudaSuccess)
+        return e;
+    constexpr int kWarps = kTcThreads / 32;
+    // registers: allocated per warp in units of 256, each of the SM's four
+    // schedulers holding a quarter of the file and of the warps
+    const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;
+    const int by_regs = regs_warp > 0 ? (regs_sm / 4 / regs_warp) * 4 / kWarps : blocks_sm;
+    const int by_smem = smem_sm / (tc_smem_bytes(MPAD, stages) + smem_rsv);
+    const int by_threads = threads_sm / kTcThreads;
+    const int by_tmem = kTmemColsPerSm / static_cast<int>(TcShape<MPAD>::kTmemCols);
+    *ctas_per_sm = std::max(0, std::min(std::min(by_regs, by_smem), std::min(std::min(by_threads, by_tmem), blocks_sm)));
+    return cudaSuccess;
+}
+
+template <int MPAD>
+cudaError_t launch_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p, int grid,
+                      bool pdl, cudaStream_t s)
+{
+    const int smem = tc_smem_bytes(MPAD, p.stages);
+    const cudaError_t e = set_tc_attrs<MPAD>();
+    if (e != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kTcThreads);
@@ -430,6 +488,17 @@ int tc_max_stages(int m_pad, int smem_limit)
     while (s > 2 && tc_smem_bytes(m_pad, s) > smem_limit)
         --s;
     return s;
+}
+
+cudaError_t tc_occupancy(int m_pad, int stages, int *ctas_per_sm)
+{
+    switch (m_pad) {
+    case 16: return occupancy_tc<16>(stages, ctas_per_sm);
+    case 32: return occupancy_tc<32>(stages, ctas_per_sm);
+    case 48: return occupancy_tc<48>(stages, ctas_per_sm);
+    case 64: return occupancy_tc<64>(stages, ctas_per_sm);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_splitk_tc(const CUtensorMap &tmW, const CUtensorMap &tmX, const TcParams &p,

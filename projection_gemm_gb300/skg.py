@@ -39,6 +39,7 @@ EXPORTS = (
     "skg_prefetch_l2", "skg_plan_set_prefetch_fraction", "skg_plan_info", "skg_plan_check",
     "skg_plan_destroy", "skg_debug_wait_timeout", "skg_last_error", "skg_version",
     "skg_run_noalloc", "skg_noalloc_check", "skg_plan_set_k_shard", "skg_combine_partials", "skg_plan_set_l2_ahead", "skg_plan_set_next_weight",
+    "skg_plan_set_reducers",
     "skg_group", "skg_group_run", "skg_group_info", "skg_group_check", "skg_group_destroy",
 )
 
@@ -58,6 +59,7 @@ class skg_plan_desc(ctypes.Structure):
         ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
         ("from_table", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
         ("prefetch_bytes", ctypes.c_size_t), ("pdl", ctypes.c_int), ("l2_ahead", ctypes.c_int),
+        ("reducers", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -97,6 +99,7 @@ def load(path: str = LIB_PATH):
     lib.skg_plan_set_k_shard.argtypes = [vp, i, i]
     lib.skg_combine_partials.argtypes = [i, i, i, P(vp), vp, vp, i, vp]
     lib.skg_plan_set_l2_ahead.argtypes = [vp, i]
+    lib.skg_plan_set_reducers.argtypes = [vp, i]
     lib.skg_plan_set_next_weight.argtypes = [vp, vp, sz]
     lib.skg_group.argtypes = [i, i, P(i), P(i), P(i), P(i), P(vp)]
     lib.skg_group_run.argtypes = [vp, P(vp), P(vp), P(vp), P(vp), vp]
@@ -176,6 +179,10 @@ def skg_plan_set_next_weight(plan: int, W_next, nbytes: int):
 
 def skg_plan_set_l2_ahead(plan: int, ahead: int):
     _check(load().skg_plan_set_l2_ahead(plan, int(ahead)))
+
+
+def skg_plan_set_reducers(plan: int, reducers: int):
+    _check(load().skg_plan_set_reducers(plan, int(reducers)))
 
 
 def skg_plan_set_prefetch_fraction(plan: int, fraction: float):
@@ -258,6 +265,9 @@ class Plan:
 
     def set_l2_ahead(self, ahead: int):
         skg_plan_set_l2_ahead(self.handle, ahead)
+
+    def set_reducers(self, reducers: int):
+        skg_plan_set_reducers(self.handle, reducers)
 
     def set_k_shard(self, rank: int, ranks: int):
         skg_plan_set_k_shard(self.handle, rank, ranks)

@@ -28,6 +28,7 @@ from .inputs import CHAIN_M, CHAIN_STAGES, DEEPK_M, SWEEP_M, WIDE_M, Projection,
 HERE = os.path.dirname(os.path.abspath(__file__))
 NOMINAL_HBM_BPS = 8.0e12   # no launch can stream its weight faster than the HBM
 INC = os.path.join(HERE, "csrc", "skg_plan_table.inc")
+REDUCER_SHAPES = 6         # fastest launch shapes of a split-K row also timed at each reducer count
 
 
 def shapes():
@@ -66,13 +67,18 @@ def candidates(M, N, K):
 
 
 def read_rows(path):
-    """The rows of an existing table file, as the tuple main() writes."""
+    """The rows of an existing table file, as the tuple main() writes:
+    (kind, M, N, K, epilogue, split, stages, grid, aux, ahead, reducers, us,
+    GB/s); a row without the reducers column reads as 0 (library default)."""
     rows = []
     pat = re.compile(r"^\{([-\d, ]+)\},\s*// ([\d.]+) us, ([\d.]+) GB/s")
     for line in open(path):
         m = pat.match(line)
         if m:
-            rows.append(tuple(int(v) for v in m.group(1).split(",")) + (float(m.group(2)), float(m.group(3))))
+            ints = tuple(int(v) for v in m.group(1).split(","))
+            if len(ints) == 10:
+                ints += (0,)
+            rows.append(ints + (float(m.group(2)), float(m.group(3))))
     return rows
 
 
@@ -88,6 +94,8 @@ def time_config(M, N, K, epi, cfg, Ws, x, res, y, rounds):
         force = {k: v for k, v in cfg.items() if k in ("split_k", "stages", "tma_burst") and v}
         p.force(**force)
         p.set_l2_ahead(cfg.get("ahead", 0))
+        if cfg.get("reducers"):
+            p.set_reducers(cfg["reducers"])
         for W in Ws[:2]:
             p.run(x, W, res, y)             # descriptors, attributes: outside the capture
         torch.cuda.synchronize()
@@ -120,11 +128,13 @@ def time_config(M, N, K, epi, cfg, Ws, x, res, y, rounds):
 
 def row_config(row):
     """A table row as the candidate dict time_config takes."""
-    kind, M, N, K, epi, split, stages, grid, aux, ahead = row[:10]
+    kind, M, N, K, epi, split, stages, grid, aux, ahead, reducers = row[:11]
     cfg = {"kind": kind, "split_k": split, "stages": stages, "ahead": ahead}
     if kind == skg.SKG_KERNEL_SPLITK_TC:
         if aux > 1:
             cfg["tma_burst"] = aux
+        if reducers:
+            cfg["reducers"] = reducers
     elif split == 1 and stages >= 2:
         cfg["tma_burst"] = aux
     return cfg
@@ -199,6 +209,8 @@ def sequence_refine(rows, log, name="sweep", steps=150, reps=3, margin_us=0.4, k
         force = {k: v for k, v in cfg.items() if k in ("split_k", "stages", "tma_burst") and v}
         p.force(**force)
         p.set_l2_ahead(cfg.get("ahead", 0))
+        if cfg.get("reducers"):
+            p.set_reducers(cfg["reducers"])
         return p
 
     def step_us(plans):
@@ -217,7 +229,7 @@ def sequence_refine(rows, log, name="sweep", steps=150, reps=3, margin_us=0.4, k
         return a.elapsed_time(b) * 1e3 / steps
 
     choice = {k: row_config(byKey[k]) for k in keys}
-    us_alone = {k: byKey[k][10] for k in keys}
+    us_alone = {k: byKey[k][11] for k in keys}
     plans = {k: plan_for(k, choice[k]) for k in keys}
     print(f"{name} step with the table: {step_us(plans):.2f} us", flush=True)
     for _ in range(passes):
@@ -256,7 +268,7 @@ def sequence_refine(rows, log, name="sweep", steps=150, reps=3, margin_us=0.4, k
             kind = cfg.get("kind", skg.SKG_KERNEL_GEMV if M <= 2 else skg.SKG_KERNEL_SPLITK_TC)
             aux = cfg.get("tma_burst", 1)
             r = (kind, M, N, K, r[4], cfg["split_k"], cfg["stages"], 0, aux, cfg.get("ahead", 0),
-                 us_alone[key], 2 * N * K / us_alone[key] / 1e3)
+                 cfg.get("reducers", 0), us_alone[key], 2 * N * K / us_alone[key] / 1e3)
         out.append(r)
     return out
 
@@ -315,13 +327,26 @@ def main(argv=None):
                     results.append((us, cfg, info))
                     log.append({"M": M, "N": N, "K": K, "epilogue": epi, "config": cfg, "us": round(us, 3),
                                 "weight_gbs": round(wbytes / us / 1e3, 1)})
+            if M > 2:
+                # reducers per tile, on the fastest launch shapes
+                best = sorted(results, key=lambda r: r[0])[:REDUCER_SHAPES]
+                for _, cfg0, info0 in best:
+                    for r in (1, 2, 4, 8):
+                        if r > cfg0["split_k"] or r == info0["reducers"]:
+                            continue
+                        cfg = dict(cfg0, reducers=r)
+                        us, info = time_config(M, N, K, epi, cfg, Ws, x, res, y, args.rounds)
+                        if us is not None:
+                            results.append((us, cfg, info))
+                            log.append({"M": M, "N": N, "K": K, "epilogue": epi, "config": cfg,
+                                        "us": round(us, 3), "weight_gbs": round(wbytes / us / 1e3, 1)})
             us, cfg, info = min(results, key=lambda r: r[0])
             kind = info["kernel_kind"]
             rows.append((kind, M, N, K, skg.EPILOGUES[epi], info["split_k"],
                          info["stages"],
                          0, info["tma_burst"] if kind == skg.SKG_KERNEL_SPLITK_TC or
                          (info["split_k"] == 1 and info["stages"] >= 2) else 1,
-                         cfg.get("ahead", 0), us, wbytes / us / 1e3))
+                         cfg.get("ahead", 0), cfg.get("reducers", 0), us, wbytes / us / 1e3))
             print(f"N={N} K={K} {epi} M={M}: best {cfg} {us:.2f} us {wbytes / us / 1e3:.0f} GB/s", flush=True)
         del Ws
         torch.cuda.empty_cache()
@@ -337,7 +362,8 @@ def write_table(path, rows, log, seconds, log_path=None):
     """The table rows (and, given log_path, the timing log) as written by main."""
     with open(path, "w") as f:
         f.write("// skg_plan_table.inc -- measured picker table.\n//\n"
-                "// Each row: { kernel_kind, M, N, K, epilogue, split_k, stages, grid, tma_burst, l2_ahead }.\n"
+                "// Each row: { kernel_kind, M, N, K, epilogue, split_k, stages, grid, tma_burst, l2_ahead,\n"
+                "// reducers } (reducers: CTAs of a split-K tile sharing its reduction, 0 = library default).\n"
                 "// stages: TC ring stages / GEMV weight-ring slots per warp (0 = library default);\n"
                 "// GEMV split 1: 0 = 16-byte loads into registers, 2 = one bulk copy per batch into\n"
                 "// a shared-memory slot of the warp, whole rows per warp, 3 = the same batches in one\n"
@@ -349,7 +375,7 @@ def write_table(path, rows, log, seconds, log_path=None):
                 "// of the batch sweep and the decode-layer chain are then chosen with their whole step\n"
                 "// timed).\n")
         for r in rows:
-            f.write("{%d, %d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.2f us, %.0f GB/s\n" % tuple(r[:12]))
+            f.write("{%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.2f us, %.0f GB/s\n" % tuple(r[:13]))
     if log_path and log:
         with open(log_path, "w") as f:
             f.write("[\n" + ",\n".join(json.dumps(r) for r in log) + "\n]\n")

@@ -15,7 +15,7 @@ _EPI = {"bf16": 0, "bf16_residual": 1, "fp32": 2}
 
 
 def table_rows():
-    """Every row of the table: (kind, M, N, K, epilogue, split, stages, grid, aux, ahead)."""
+    """Every row of the table: (kind, M, N, K, epilogue, split, stages, grid, aux, ahead, reducers)."""
     rows = []
     for line in open(_INC):
         m = re.match(r"^\{([-\d, ]+)\}", line)

@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
     lib = skg.load()
     for name in header_symbols():
         assert hasattr(lib, name), name
-    assert skg.skg_version() == 2
+    assert skg.skg_version() == 3
 
 
 def test_library_is_sm103a_only():
@@ -54,8 +54,9 @@ def test_kernel_kind_follows_batch(M):
         assert d["grid"] == 56 * s
         assert d["workspace_bytes"] == s * M * 7168 * 4 + 56 * 4
         assert d["smem_bytes"] <= 232448
+        assert d["reducers"] in (1, 2, 4, 8)
     else:
-        assert d["workspace_bytes"] == 0
+        assert d["workspace_bytes"] == 0 and d["reducers"] == 0
 
 
 @pytest.mark.parametrize("N,K,epi", [(384, 7168, "fp32"), (12288, 7168, "bf16"), (7168, 16384, "bf16_residual"),
@@ -130,7 +131,7 @@ def test_plan_table_rows_are_well_formed():
     assert rows
     keys = [(r[1], r[2], r[3], r[4]) for r in rows]
     assert len(keys) == len(set(keys))
-    for kind, M, N, K, epi, split, stages, grid, burst, ahead, us, gbs in rows:
+    for kind, M, N, K, epi, split, stages, grid, burst, ahead, reducers, us, gbs in rows:
         assert kind in (skg.SKG_KERNEL_GEMV, skg.SKG_KERNEL_SPLITK_TC)
         assert 1 <= M <= 64 and N >= 1 and K % 8 == 0 and epi in (0, 1, 2)
         assert split & (split - 1) == 0 and 16 % split == 0
@@ -138,6 +139,7 @@ def test_plan_table_rows_are_well_formed():
             assert M <= 2 and split <= 8
         else:
             assert split >= 2 and 2 <= stages <= 16 and burst >= 1 and 0 <= ahead <= 64
+            assert reducers in (0, 1, 2, 4, 8) and reducers <= split
         assert us > 0 and 0 < gbs < 8000          # no launch streams faster than the HBM
         epi_name = {0: "bf16", 1: "bf16_residual", 2: "fp32"}[epi]
         d = skg.skg_plan_query(M, N, K, epi_name, SMS, L2)

@@ -25,6 +25,7 @@ pytestmark = pytest.mark.gpu
 
 GEMV_SPLITS = (1, 2, 4, 8)
 TC_SPLITS = (2, 4, 8, 16)
+REDUCERS = (1, 2, 4, 8)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -36,9 +37,10 @@ def _lib():
 
 
 def force_each_split(case: DeviceCase, base, M):
-    """Run every split the plan accepts; each must reproduce `base` exactly.
-    The GEMV rejects splits whose per-warp K slice exceeds its register
-    budget (SKG_ERR_UNSUPPORTED); those are skipped."""
+    """Run every split the plan accepts (the split-K kernel at every reducer
+    count per tile); each must reproduce `base` exactly.  The GEMV rejects
+    splits whose per-warp K slice exceeds its register budget
+    (SKG_ERR_UNSUPPORTED); those are skipped."""
     ran = []
     for s in (GEMV_SPLITS if M <= 2 else TC_SPLITS):
         try:
@@ -46,8 +48,11 @@ def force_each_split(case: DeviceCase, base, M):
         except skg.SkgError as e:
             assert e.status == skg.SKG_ERR_UNSUPPORTED, e
             continue
-        got = case.run_bits()
-        assert np.array_equal(got, base), f"split {s} changed the bits of {case.p}"
+        for r in (REDUCERS if case.plan.info()["kernel"] == "splitk_tc" else (None,)):
+            if r:
+                case.plan.set_reducers(r)
+            got = case.run_bits()
+            assert np.array_equal(got, base), f"split {s}, reducers {r} changed the bits of {case.p}"
         ran.append(s)
     return ran
 
@@ -279,6 +284,25 @@ def test_full_size_splits_bit_identical(M):
         case.close()
 
 
+@pytest.mark.parametrize("M", (8, 64))
+def test_chain_reducers_bit_identical(M):
+    """The decode-layer chain's split-K stages at every reducer count per
+    tile: the bits of the default plan, which meet the oracle."""
+    for p in chain(M):
+        case = DeviceCase(p)
+        try:
+            if case.plan.info()["kernel"] != "splitk_tc":
+                continue
+            base = case.run_bits()
+            full_check(case, base, what=f"{p.name} default reducers")
+            for r in REDUCERS:
+                case.plan.set_reducers(r)
+                assert np.array_equal(case.run_bits(), base), f"{p.name}: reducers {r} changed the bits"
+            case.plan.check()
+        finally:
+            case.close()
+
+
 # ---------------------------------------------------------------- errors
 def test_rejections_launch_nothing():
     p = skg.Plan(4, 256, 256, "bf16")
@@ -325,6 +349,41 @@ def test_force_kernel_rejections_keep_the_plan():
         case.plan.check()
     finally:
         case.close()
+
+
+def test_reducer_rejections_and_bounds():
+    """Reducers per tile: 1, 2, 4 or 8 on a split-K plan; a GEMV plan rejects
+    them; the plan reports the count a launch uses -- at most the split, and
+    few enough that the waiting CTAs stay fewer than the SMs hold."""
+    tc = skg.Plan(64, 7168, 4096, "bf16")
+    gemv = skg.Plan(1, 7168, 4096, "bf16")
+    try:
+        gemv.force_kernel(skg.SKG_KERNEL_GEMV)
+        for bad in (0, 3, 16, -1):
+            with pytest.raises(skg.SkgError) as e:
+                tc.set_reducers(bad)
+            assert e.value.status == skg.SKG_ERR_INVALID_ARG
+        with pytest.raises(skg.SkgError) as e:
+            gemv.set_reducers(2)
+        assert e.value.status == skg.SKG_ERR_UNSUPPORTED
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        tc.force(split_k=4)
+        tc.set_reducers(8)
+        assert tc.info()["reducers"] == 4                       # at most the split
+        tc.force(split_k=16)
+        tc.set_reducers(8)
+        assert tc.info()["reducers"] == 1                       # splits of 16 reduce in one CTA
+        tc.force(split_k=8, stages=4)
+        # m_pad 64, a 4-stage ring: registers, shared memory and TMEM each
+        # allow 2 CTAs per SM (the profiler's launch statistics agree)
+        assert tc.info()["ctas_per_sm"] == 2
+        tc.set_reducers(8)
+        # 56 tiles; m_pad 64 holds 2 CTAs per SM: the largest R with 56 x (R - 1) < 2 x SMs
+        r = tc.info()["reducers"]
+        assert r in (1, 2, 4, 8) and 56 * (r - 1) < 2 * sms and (r == 8 or 56 * (2 * r - 1) >= 2 * sms)
+    finally:
+        tc.close()
+        gemv.close()
 
 
 def test_table_rows_launch_what_the_tuner_measured():
