@@ -153,57 +153,70 @@ def measured_hbm_gbs():
 SEQUENCES = {
     "sweep": lambda: [(M, 7168, 7168, "bf16") for M in SWEEP_M],
     "chain": lambda: [(M, N, K, epi) for M in CHAIN_M for (K, N, epi) in CHAIN_STAGES],
+    "wide": lambda: [(M, 12288, 7168, "bf16") for M in WIDE_M],
+    "deepk": lambda: [(M, 7168, 16384, "bf16_residual") for M in DEEPK_M],
 }
 
 
-def sequence_refine(rows, log, name="sweep", steps=150, reps=3, margin_us=0.4, keep=8, bar_margin=0.02,
+def sequence_refine(rows, log, names=("sweep",), steps=150, reps=3, margin_us=0.4, keep=8, bar_margin=0.02,
                     passes=2):
     """The projections of a workload's step always run as one sequence (the
     batch sweep M = 1, 2, ..., 64; the decode layer's five stages at M = 1, 8,
-    64), and a launch's best configuration alone is not always its best next
-    to the others: a neighbour with another shared-memory footprint starts
-    later, and the next launch's look-ahead requests meet this launch's
-    latency-bound reduction in L2.  Coordinate descent over each projection's
-    `keep` fastest launch shapes alone (with look-ahead 0 to 4 each), timing
-    whole eager steps; a change is kept only if it beats the incumbent, timed
-    alternately, by margin_us per step in every one of `reps` pairs, and only
-    among launch shapes whose time alone still clears the projection's
-    roofline bar (0.80 at M <= 16, 0.70 above) by bar_margin.  Returns the
-    rows with the sequence's entries replaced."""
-    seq = SEQUENCES[name]()
+    64; the wide and deep-K batches), and a launch's best configuration alone
+    is not always its best next to the others: a neighbour with another
+    shared-memory footprint starts later, and the next launch's look-ahead
+    requests meet this launch's latency-bound reduction in L2.  Coordinate
+    descent over each projection's `keep` fastest launch shapes alone (with
+    look-ahead 0 to 4 each), timing whole eager steps of every named
+    workload that holds the projection (a shape shared by two workloads, such
+    as the 12288-wide projection of the chain and of the wide batch, is
+    judged by the sum of their steps); a change is kept only if it beats the
+    incumbent, timed alternately, by margin_us in every one of `reps` pairs,
+    and only among launch shapes whose time alone still clears the
+    projection's roofline bar (0.80 at M <= 16, 0.70 above) by bar_margin.
+    Returns the rows with the sequences' entries replaced."""
+    if isinstance(names, str):
+        names = (names,)
     byKey = {(r[1], r[2], r[3], r[4]): r for r in rows}
-    keys = [(M, N, K, skg.EPILOGUES[epi]) for M, N, K, epi in seq]
+    seq_keys = {n: [(M, N, K, skg.EPILOGUES[epi]) for M, N, K, epi in SEQUENCES[n]()] for n in names}
+    keys = []
+    for n in names:
+        keys += [k for k in seq_keys[n] if k not in keys]
+    holders = {k: [n for n in names if k in seq_keys[n]] for k in keys}
+    epi_name = {v: k for k, v in skg.EPILOGUES.items()}
     cands = {}
-    for (M, N, K, epi) in seq:
-        entries = sorted((e for e in log if (e["M"], e["N"], e["K"], e["epilogue"]) == (M, N, K, epi)
-                          and (M > 2 or "kind" in e["config"])), key=lambda e: e["us"])
+    for key in keys:
+        M, N, K, e = key
+        entries = sorted((x for x in log if (x["M"], x["N"], x["K"], skg.EPILOGUES[x["epilogue"]]) == key
+                          and (M > 2 or "kind" in x["config"])), key=lambda x: x["us"])
         shapes_, c, seen = [], [], set()
-        for e in entries:
-            shape = json.dumps({k: v for k, v in e["config"].items() if k != "ahead"}, sort_keys=True)
+        for x in entries:
+            shape = json.dumps({k: v for k, v in x["config"].items() if k != "ahead"}, sort_keys=True)
             if shape not in shapes_:
                 shapes_.append(shape)
         for shape in shapes_[:keep]:
-            for e in entries:
-                cfg = e["config"]
-                key = json.dumps(cfg, sort_keys=True)
+            for x in entries:
+                cfg = x["config"]
+                ck = json.dumps(cfg, sort_keys=True)
                 if (json.dumps({k: v for k, v in cfg.items() if k != "ahead"}, sort_keys=True) == shape
-                        and cfg.get("ahead", 0) <= 4 and key not in seen):
-                    seen.add(key)
-                    c.append((cfg, e["us"]))
+                        and cfg.get("ahead", 0) <= 4 and ck not in seen):
+                    seen.add(ck)
+                    c.append((cfg, x["us"]))
         bar = (0.80 if M <= 16 else 0.70) + bar_margin
-        p = Projection(M, N, K, epi)
-        ideal_us = p.algorithmic_bytes() / (measured_hbm_gbs() * 1e3)
-        cands[(M, N, K, skg.EPILOGUES[epi])] = [(cfg, us) for cfg, us in c if ideal_us / us >= bar]
-    ops = []
-    for i, (M, N, K, epi) in enumerate(seq):
-        t = generate(Projection(M, N, K, epi, seed=950 + i))
-        ops.append(dict(W=t.W.cuda(), x=t.x.cuda(), res=None if t.res is None else t.res.cuda(),
-                        y=torch.empty(M, N, dtype=torch.float32 if epi == "fp32" else torch.bfloat16,
-                                      device="cuda")))
+        ideal_us = Projection(M, N, K, epi_name[e]).algorithmic_bytes() / (measured_hbm_gbs() * 1e3)
+        cands[key] = [(cfg, us) for cfg, us in c if ideal_us / us >= bar]
+    ops = {}
+    for n in names:
+        ops[n] = []
+        for i, (M, N, K, epi) in enumerate(SEQUENCES[n]()):
+            t = generate(Projection(M, N, K, epi, seed=950 + i))
+            ops[n].append(dict(W=t.W.cuda(), x=t.x.cuda(), res=None if t.res is None else t.res.cuda(),
+                               y=torch.empty(M, N, dtype=torch.float32 if epi == "fp32" else torch.bfloat16,
+                                             device="cuda")))
 
     def plan_for(key, cfg):
-        M, N, K, epi = key
-        p = skg.Plan(M, N, K, epi)
+        M, N, K, e = key
+        p = skg.Plan(M, N, K, epi_name[e])
         if cfg.get("kind"):
             p.force_kernel(cfg["kind"])
         force = {k: v for k, v in cfg.items() if k in ("split_k", "stages", "tma_burst") and v}
@@ -213,9 +226,9 @@ def sequence_refine(rows, log, name="sweep", steps=150, reps=3, margin_us=0.4, k
             p.set_reducers(cfg["reducers"])
         return p
 
-    def step_us(plans):
+    def step_us(plans, n):
         def one():
-            for key, o in zip(keys, ops):
+            for key, o in zip(seq_keys[n], ops[n]):
                 plans[key].run(o["x"], o["W"], o["res"], o["y"])
         for _ in range(3):
             one()
@@ -228,12 +241,17 @@ def sequence_refine(rows, log, name="sweep", steps=150, reps=3, margin_us=0.4, k
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e3 / steps
 
+    def total_us(plans, ns):
+        return sum(step_us(plans, n) for n in ns)
+
     choice = {k: row_config(byKey[k]) for k in keys}
     us_alone = {k: byKey[k][11] for k in keys}
     plans = {k: plan_for(k, choice[k]) for k in keys}
-    print(f"{name} step with the table: {step_us(plans):.2f} us", flush=True)
+    for n in names:
+        print(f"{n} step with the table: {step_us(plans, n):.2f} us", flush=True)
     for _ in range(passes):
         for key in keys:
+            ns = holders[key]
             for cfg, us in cands[key]:
                 if cfg == choice[key]:
                     continue
@@ -245,18 +263,19 @@ def sequence_refine(rows, log, name="sweep", steps=150, reps=3, margin_us=0.4, k
                 wins = 0
                 for _ in range(reps):
                     plans[key] = incumbent
-                    t_inc = step_us(plans)
+                    t_inc = total_us(plans, ns)
                     plans[key] = trial
-                    t_new = step_us(plans)
+                    t_new = total_us(plans, ns)
                     wins += t_new < t_inc - margin_us
                 if wins == reps:
                     incumbent.close()
                     choice[key], us_alone[key] = cfg, us
-                    print(f"  {key}: {cfg} ({t_new:.2f} against {t_inc:.2f} us per step)", flush=True)
+                    print(f"  {key}: {cfg} ({t_new:.2f} against {t_inc:.2f} us, steps {'+'.join(ns)})", flush=True)
                 else:
                     trial.close()
                     plans[key] = incumbent
-    print(f"{name} step chosen in sequence: {step_us(plans):.2f} us", flush=True)
+    for n in names:
+        print(f"{n} step chosen in sequence: {step_us(plans, n):.2f} us", flush=True)
     for p in plans.values():
         p.close()
     out = []
@@ -281,7 +300,7 @@ def main(argv=None):
     ap.add_argument("--only-m", type=int, nargs="*", default=None,
                     help="tune only these M; the table's rows (and the log's entries) for other M are kept")
     ap.add_argument("--sequence", nargs="*", choices=sorted(SEQUENCES), default=None,
-                    help="then refine these workloads' rows with their whole step timed (sequence_refine)")
+                    help="then refine these workloads' rows with their whole steps timed (sequence_refine)")
     ap.add_argument("--sequence-only", nargs="+", choices=sorted(SEQUENCES), default=None,
                     help="only refine these workloads' rows of the existing table in sequence (uses --out-log's "
                          "timings alone)")
@@ -292,8 +311,7 @@ def main(argv=None):
         torch.cuda.set_device(0)
         rows = [tuple(r) for r in read_rows(args.out_inc)]
         log = json.load(open(args.out_log or os.path.join(HERE, "csrc", "skg_plan_tune_log.json")))
-        for name in args.sequence_only:
-            rows = sequence_refine(rows, log, name)
+        rows = sequence_refine(rows, log, tuple(args.sequence_only))
         write_table(args.out_inc, rows, None, 0.0)
         return
     kept_rows, kept_log = [], []
@@ -352,8 +370,8 @@ def main(argv=None):
         torch.cuda.empty_cache()
     rows = sorted(kept_rows + rows, key=lambda r: (r[2], r[3], r[4], r[1]))
     log = kept_log + log
-    for name in (args.sequence or []):
-        rows = sequence_refine(rows, log, name)
+    if args.sequence:
+        rows = sequence_refine(rows, log, tuple(args.sequence))
     write_table(args.out_inc, rows, args.out_log and log, time.time() - t0, args.out_log)
     print(f"wrote {args.out_inc} ({len(rows)} rows)")
 
@@ -372,8 +390,8 @@ def write_table(path, rows, log, seconds, log_path=None):
                 f"// from back-to-back timings on {torch.cuda.get_device_name(0)} "
                 f"({len(rows)} rows); the comment on each row is the\n"
                 "// measured time per launch and weight-stream rate (launches of that row alone; the rows\n"
-                "// of the batch sweep and the decode-layer chain are then chosen with their whole step\n"
-                "// timed).\n")
+                "// of the batch sweep, the decode-layer chain and the wide and deep-K batches are then\n"
+                "// chosen with their whole steps timed).\n")
         for r in rows:
             f.write("{%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.2f us, %.0f GB/s\n" % tuple(r[:13]))
     if log_path and log:
