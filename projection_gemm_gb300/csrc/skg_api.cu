@@ -470,6 +470,7 @@ struct skg_plan_s {
     void *ws = nullptr;               // [S][tiles][M][128] fp32 partials, then counters
     size_t ws_cap = 0;
     std::vector<void *> retired;      // outgrown workspaces: a captured graph may still use them
+    int want_reducers = 0;            // requested reducers per tile (table, default or skg_plan_set_reducers)
     int occ_m_pad = 0, occ_stages = 0; // shape of the split-K launch tc_ctas_per_sm was measured for
     int tc_ctas_per_sm = 1;
     const void *next_w = nullptr;     // prefetched into L2 by this plan's launches
@@ -549,6 +550,29 @@ skg_status skg_plan_query(int M, int N, int K, int epilogue, int num_sms, size_t
     return query(M, N, K, epilogue, num_sms, l2_bytes, out);
 }
 
+// After any change of a plan's launch shape: the reducers per tile its
+// launches use (the requested count within the bound of safe_reducers, for
+// this shape's occupancy), then the workspace for the shape.
+skg_status finish_update(skg_plan_t p)
+{
+    if (p->d.kernel_kind == SKG_KERNEL_SPLITK_TC) {
+        if (p->occ_m_pad != p->d.m_pad || p->occ_stages != p->d.stages) {
+            int occ = 1;
+            const cudaError_t e = tc_occupancy(p->d.m_pad, p->d.stages, &occ);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "split-K occupancy");
+            p->occ_m_pad = p->d.m_pad;
+            p->occ_stages = p->d.stages;
+            p->tc_ctas_per_sm = std::max(1, occ);
+        }
+        const int n_tiles = (p->d.N + kTileN - 1) / kTileN;
+        p->d.reducers = safe_reducers(p->want_reducers, n_tiles, p->d.split_k, p->num_sms * p->tc_ctas_per_sm);
+    } else {
+        p->d.reducers = 0;
+    }
+    return ensure_workspace(p);
+}
+
 skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out)
 {
     if (!out)
@@ -605,7 +629,8 @@ skg_status skg_plan(int M, int N, int K, int epilogue, skg_plan_t *out)
         delete p;
         return cuda_fail(e, "cudaHostGetDevicePointer(error word)");
     }
-    st = ensure_workspace(p);
+    p->want_reducers = p->d.reducers;
+    st = finish_update(p);
     if (st != SKG_OK) {
         skg_plan_destroy(p);
         return st;
@@ -689,7 +714,7 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int t
     p->d = d;
     p->wmaps.clear();
     p->xmaps.clear();
-    return ensure_workspace(p);
+    return finish_update(p);
 }
 
 skg_status skg_plan_force_kernel(skg_plan_t p, int kind)
@@ -717,9 +742,10 @@ skg_status skg_plan_force_kernel(skg_plan_t p, int kind)
     if (p->k_ranks > 1 && d.split_k > kChunks / p->k_ranks)
         fill_tc(&d, kChunks / p->k_ranks, d.stages, d.tma_burst);
     p->d = d;
+    p->want_reducers = d.reducers;   // re-planned: the new shape's default
     p->wmaps.clear();
     p->xmaps.clear();
-    return ensure_workspace(p);
+    return finish_update(p);
 }
 
 skg_status skg_plan_set_k_shard(skg_plan_t p, int rank, int ranks)
@@ -738,7 +764,8 @@ skg_status skg_plan_set_k_shard(skg_plan_t p, int rank, int ranks)
                         p->d.K, kChunks * kBlockK);
     }
     skg_plan_desc d = p->d;
-    if (ranks > 1 && d.kernel_kind != SKG_KERNEL_SPLITK_TC) {
+    const bool replan = ranks > 1 && d.kernel_kind != SKG_KERNEL_SPLITK_TC;
+    if (replan) {
         const skg_status st = query(d.M, d.N, d.K, d.epilogue, p->num_sms, p->l2_bytes, &d, SKG_KERNEL_SPLITK_TC);
         if (st != SKG_OK)
             return st;
@@ -747,12 +774,14 @@ skg_status skg_plan_set_k_shard(skg_plan_t p, int rank, int ranks)
     if (d.kernel_kind == SKG_KERNEL_SPLITK_TC && d.split_k > kChunks / ranks)
         fill_tc(&d, kChunks / ranks, d.stages, d.tma_burst);   // a rank's CTAs split its chunks
     p->d = d;
+    if (replan)
+        p->want_reducers = d.reducers;
     p->k_rank = rank;
     p->k_ranks = ranks;
     refresh_prefetch_bytes(p);
     p->wmaps.clear();
     p->xmaps.clear();
-    return ensure_workspace(p);
+    return finish_update(p);
 }
 
 skg_status skg_combine_partials(int M, int N, int ranks, const float *const *partials, const void *residual,
@@ -817,15 +846,8 @@ skg_status skg_plan_set_reducers(skg_plan_t p, int reducers)
         return fail(SKG_ERR_INVALID_ARG, "reducers=%d must be 1, 2, 4 or 8", reducers);
     if (p->d.kernel_kind != SKG_KERNEL_SPLITK_TC)
         return fail(SKG_ERR_UNSUPPORTED, "reducers apply to the split-K kernel only");
-    // the count a launch of the current shape uses (skg_run applies the same
-    // bound again after any later change of the shape)
-    int occ = 1;
-    const cudaError_t e = tc_occupancy(p->d.m_pad, p->d.stages, &occ);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    const int n_tiles = (p->d.N + kTileN - 1) / kTileN;
-    p->d.reducers = safe_reducers(reducers, n_tiles, p->d.split_k, p->num_sms * std::max(1, occ));
-    return SKG_OK;
+    p->want_reducers = reducers;
+    return finish_update(p);
 }
 
 skg_status skg_plan_set_prefetch_fraction(skg_plan_t p, double fraction)
@@ -844,13 +866,7 @@ skg_status skg_plan_info(skg_plan_t p, skg_plan_desc *out)
     if (!p || !out)
         return fail(SKG_ERR_INVALID_ARG, "skg_plan_info: NULL argument");
     *out = p->d;
-    int occ = p->gemv_ctas_per_sm;
-    if (p->d.kernel_kind == SKG_KERNEL_SPLITK_TC) {
-        const cudaError_t e = tc_occupancy(p->d.m_pad, p->d.stages, &occ);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    }
-    out->ctas_per_sm = occ;
+    out->ctas_per_sm = p->d.kernel_kind == SKG_KERNEL_SPLITK_TC ? p->tc_ctas_per_sm : p->gemv_ctas_per_sm;
     return SKG_OK;
 }
 
@@ -929,16 +945,7 @@ skg_status skg_run(skg_plan_t p, const void *x, const void *W, const void *resid
         t.next_bytes = p->next_bytes;
         t.epilogue = d.epilogue;
         t.timeout_ns = kDefaultTimeoutNs;
-        if (p->occ_m_pad != d.m_pad || p->occ_stages != d.stages) {
-            int occ = 1;
-            e = tc_occupancy(d.m_pad, d.stages, &occ);
-            if (e != cudaSuccess)
-                return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-            p->occ_m_pad = d.m_pad;
-            p->occ_stages = d.stages;
-            p->tc_ctas_per_sm = std::max(1, occ);
-        }
-        t.reducers = safe_reducers(d.reducers, n_tiles, d.split_k, p->num_sms * p->tc_ctas_per_sm);
+        t.reducers = d.reducers;      // bounded for this launch shape whenever the shape changed
         t.chunk_count = kChunks / p->k_ranks;
         t.chunk_base = p->k_rank * t.chunk_count;
         e = launch_splitk_tc(*mw, *mx, t, d.m_pad, d.grid, d.pdl != 0, s);

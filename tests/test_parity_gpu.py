@@ -386,6 +386,27 @@ def test_reducer_rejections_and_bounds():
         gemv.close()
 
 
+def test_table_reducers_reach_the_plan():
+    """A split-K table row's reducers per tile are what the plan launches,
+    within the bound on waiting CTAs (tiles x (R - 1) below the CTAs the SMs
+    hold) for the row's launch shape."""
+    from tests.plan_table import table_rows
+    rows = [r for r in table_rows() if r[0] == skg.SKG_KERNEL_SPLITK_TC]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for kind, M, N, K, epi, split, stages, grid, aux, ahead, reducers in rows:
+        p = skg.Plan(M, N, K, epi)
+        try:
+            i = p.info()
+            assert i["from_table"] == 1 and i["ctas_per_sm"] >= 1
+            want = reducers if reducers else (2 if M > 16 else 1)
+            r = min(want, split) if split <= 8 else 1
+            while r > 1 and -(-N // 128) * (r - 1) >= sms * i["ctas_per_sm"]:
+                r //= 2
+            assert i["reducers"] == r, (M, N, K, i["reducers"], r)
+        finally:
+            p.close()
+
+
 def test_table_rows_launch_what_the_tuner_measured():
     """A measured GEMV row whose warps share rows (split > 1) leaves the grid
     to the library: the plan must launch the grid the tuner timed, one wave
@@ -394,7 +415,7 @@ def test_table_rows_launch_what_the_tuner_measured():
     from tests.plan_table import table_rows
     rows = [r for r in table_rows() if r[0] == skg.SKG_KERNEL_GEMV and r[5] > 1 and r[7] == 0]
     assert rows, "no GEMV row with warps sharing rows to check"
-    for kind, M, N, K, epi, split, stages, grid, aux, ahead in rows:
+    for kind, M, N, K, epi, split, stages, grid, aux, ahead, _reducers in rows:
         a = skg.Plan(M, N, K, epi)
         b = skg.Plan(M, N, K, epi)
         try:
