@@ -112,7 +112,7 @@ typedef struct skg_plan_desc {
                                batches of the row; 0 = none */
     int reducers;           /* TC: the last `reducers` CTAs to finish a tile share its final
                                reduction (1, 2, 4 or 8; a launch uses fewer where the split is
-                               smaller or the waiting CTAs could fill the SMs); GEMV: 0 */
+                               smaller, and 1 where its grid is more than one wave); GEMV: 0 */
     int ctas_per_sm;        /* CTAs one SM holds at once: TC, the CUDA occupancy calculator for
                                this launch shape; GEMV, the count the plan sizes one-wave grids
                                from.  Filled by skg_plan_info; 0 from skg_plan_query */
@@ -264,10 +264,11 @@ SKG_API skg_status skg_plan_set_l2_ahead(skg_plan_t plan, int ahead);
  * canonical tree, the residual added, one rounding) is done by the last R
  * CTAs of the tile to finish, each taking 1/R of the tile's outputs; all but
  * the last wait, with the plan's bounded wait, for the others.  R = 1, 2, 4
- * or 8.  The output bits do not depend on R.  A launch uses min(R, split_k)
- * (1 at split 16), halved until tiles x (R - 1) waiting CTAs are fewer than
- * the CTAs the SMs hold at once; the plan's description reports that count
- * for its current launch shape.  Errors: SKG_ERR_INVALID_ARG (R),
+ * or 8.  The output bits do not depend on R.  A launch uses min(R, split_k),
+ * and 1 at split 16 or while its grid is more than one wave of the CTAs the
+ * SMs hold at once (within one wave the waiting CTAs always leave the CTAs
+ * they wait for a place); the plan's description reports that count for its
+ * current launch shape.  Errors: SKG_ERR_INVALID_ARG (R),
  * SKG_ERR_UNSUPPORTED (a GEMV plan), SKG_ERR_CUDA.
  */
 SKG_API skg_status skg_plan_set_reducers(skg_plan_t plan, int reducers);

@@ -263,30 +263,42 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
     } else {
         int split, stages = 0, burst = 1;
         const int n_tiles = (N + kTileN - 1) / kTileN;
-        // measured default: at M > 16 the partials take a lone reducer two
-        // rounds of loads, and two reducers per tile save 1 to 2 us a launch
-        // at M = 64; at M <= 16 the wait costs more than it saves
-        d->reducers = M > 16 ? 2 : 1;
         if (row) {
             split = row->split;
             stages = row->stages;
             burst = row->burst;
             d->l2_ahead = row->ahead;
-            if (row->reducers > 0)
-                d->reducers = row->reducers;
             d->from_table = 1;
         } else {
-            // Measured on GB300 (back-to-back launches): about 1.5 CTAs per
-            // SM with a 4-6 stage ring streams best; deeper rings at one CTA
-            // per SM and grids beyond one wave both lose.
+            // Measured on GB300 (the tuned rows and 48 shapes outside the
+            // table, back-to-back launches): the fastest launches split K as
+            // finely as one wave of CTAs at the ring's occupancy holds (at
+            // most 8 ways, no finer than the chunks K has), with a short ring:
+            // m_pad 16 takes 4 stages (3 CTAs per SM) or 6 (2 per SM), m_pad
+            // 32 3 stages (3 per SM) or 4 (2 per SM) -- the deeper ring
+            // wherever 2 CTAs per SM hold the same split in one wave -- and
+            // m_pad 48 and 64 4 stages (2 per SM).  One CTA per SM with a
+            // deep ring and grids beyond one wave both lose.
             const int mp = (M + 15) / 16 * 16;
-            stages = mp <= 16 ? 6 : (mp <= 48 ? 5 : 4);
-            stages = std::min(stages, tc_max_stages(mp, 232448));
-            d->l2_ahead = 2;   // measured: 2-4 tiles after the ring into L2 before the wait
-            split = 2;
-            while (split < kChunks && n_tiles * split * 2 <= num_sms * 8 / 5)
-                split *= 2;
+            const int present = chunks_present((K + kBlockK - 1) / kBlockK);
+            auto split_for = [&](int per_sm) {
+                int sp = 2;
+                while (sp < 8 && static_cast<long long>(n_tiles) * sp * 2 <= static_cast<long long>(num_sms) * per_sm &&
+                       sp * 2 <= present)
+                    sp *= 2;
+                return sp;
+            };
+            const int s3 = split_for(3), s2 = split_for(2);
+            const bool deep = mp > 32 || (s2 == s3 && static_cast<long long>(n_tiles) * s2 <= 2ll * num_sms);
+            split = deep ? s2 : s3;
+            stages = mp == 16 ? (deep ? 6 : 4) : (mp == 32 ? (deep ? 4 : 3) : 4);
+            d->l2_ahead = 2;   // measured: 2 tiles after the ring into L2 before the wait
         }
+        // Reducers per tile: the row's, else the measured default -- from
+        // M = 16 four reducers beat one wherever a tile's split is 4 or 8 and
+        // the tiles are few (<= 56); with more tiles, or shorter splits, the
+        // waits cost more than the shorter reduction saves.
+        d->reducers = (row && row->reducers > 0) ? row->reducers : ((M >= 16 && split >= 4 && n_tiles <= 56) ? 4 : 1);
         fill_tc(d, split, stages, burst);
     }
     return SKG_OK;
@@ -362,19 +374,18 @@ struct MapCache {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// The reducers per tile a launch may use: at most the plan's R, the split
-// (splits of 16 reduce in one CTA), and few enough that the waiting CTAs,
-// tiles x (R - 1), stay fewer than the CTAs the SMs hold at once
-// (`slots`): every other CTA runs to completion without waiting, so the
-// CTAs a waiter waits for always get an SM.
+// The reducers per tile a launch may use: at most the plan's R and the
+// split (splits of 16 reduce in one CTA), and none but the last arrival
+// while the grid, tiles x split, is more than one wave of the CTAs the SMs
+// hold at once (`slots`; a waiter would wait for CTAs of a later wave,
+// measured 25% slower on a two-wave launch).  Within one wave the waiting
+// CTAs, tiles x (R - 1), are fewer than the slots, so every CTA a waiter
+// waits for -- one that never waits -- always has an SM.
 int safe_reducers(int want, int n_tiles, int split, int slots)
 {
-    if (split > 8)
+    if (split > 8 || static_cast<long long>(n_tiles) * split > slots)
         return 1;
-    int r = std::max(1, std::min(want, split));
-    while (r > 1 && static_cast<long long>(n_tiles) * (r - 1) >= slots)
-        r /= 2;
-    return r;
+    return std::max(1, std::min(want, split));
 }
 
 } // namespace

@@ -53,9 +53,9 @@ namespace {
 // (acquire, GPU scope) until all `target` arrivals are in, for at most
 // timeout_ns, or until another role of the CTA gave up.  Every CTA arrives
 // before it waits, so a waiter waits only for CTAs that never wait; the host
-// allows R reducers per tile only while the waiters, tiles x (R - 1), are
-// fewer than the CTAs the SMs hold at once, so a CTA waited for always finds
-// a free slot.
+// allows R > 1 reducers per tile only while the whole grid is one wave of
+// the CTAs the SMs hold at once, so the waiters, tiles x (R - 1), are fewer
+// than the slots and a CTA waited for always finds one.
 __device__ __forceinline__ bool wait_arrivals(const unsigned *ctr, unsigned target, uint64_t timeout_ns,
                                               volatile int *abort)
 {

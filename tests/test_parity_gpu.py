@@ -354,7 +354,7 @@ def test_force_kernel_rejections_keep_the_plan():
 def test_reducer_rejections_and_bounds():
     """Reducers per tile: 1, 2, 4 or 8 on a split-K plan; a GEMV plan rejects
     them; the plan reports the count a launch uses -- at most the split, and
-    few enough that the waiting CTAs stay fewer than the SMs hold."""
+    1 while the grid is more than one wave of the CTAs the SMs hold."""
     tc = skg.Plan(64, 7168, 4096, "bf16")
     gemv = skg.Plan(1, 7168, 4096, "bf16")
     try:
@@ -378,12 +378,19 @@ def test_reducer_rejections_and_bounds():
         # allow 2 CTAs per SM (the profiler's launch statistics agree)
         assert tc.info()["ctas_per_sm"] == 2
         tc.set_reducers(8)
-        # 56 tiles; m_pad 64 holds 2 CTAs per SM: the largest R with 56 x (R - 1) < 2 x SMs
-        r = tc.info()["reducers"]
-        assert r in (1, 2, 4, 8) and 56 * (r - 1) < 2 * sms and (r == 8 or 56 * (2 * r - 1) >= 2 * sms)
+        assert 56 * 8 > 2 * sms and tc.info()["reducers"] == 1    # 448 CTAs: more than one wave
+        tc.force(split_k=4)
+        assert tc.info()["reducers"] == 4                       # 224 CTAs: one wave, the request returns
     finally:
         tc.close()
         gemv.close()
+    narrow = skg.Plan(64, 4096, 4096, "bf16")
+    try:
+        narrow.force(split_k=8, stages=4)
+        narrow.set_reducers(8)
+        assert narrow.info()["reducers"] == 8                   # 32 tiles x 8: one wave
+    finally:
+        narrow.close()
 
 
 def test_table_reducers_reach_the_plan():
@@ -398,10 +405,9 @@ def test_table_reducers_reach_the_plan():
         try:
             i = p.info()
             assert i["from_table"] == 1 and i["ctas_per_sm"] >= 1
-            want = reducers if reducers else (2 if M > 16 else 1)
-            r = min(want, split) if split <= 8 else 1
-            while r > 1 and -(-N // 128) * (r - 1) >= sms * i["ctas_per_sm"]:
-                r //= 2
+            tiles, slots = -(-N // 128), sms * i["ctas_per_sm"]
+            want = reducers if reducers else (4 if M >= 16 and split >= 4 and tiles <= 56 else 1)
+            r = min(want, split) if split <= 8 and tiles * split <= slots else 1
             assert i["reducers"] == r, (M, N, K, i["reducers"], r)
         finally:
             p.close()
