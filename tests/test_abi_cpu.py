@@ -111,6 +111,30 @@ def test_default_rule_for_shapes_outside_the_table(N, K):
     assert d8["from_table"] == 0 and d8["kernel"] == "splitk_tc" and d8["l2_ahead"] == 2
 
 
+@pytest.mark.parametrize("M,N,K,split,stages,reducers", [
+    (8, 5120, 5120, 8, 4, 1),      # 40 tiles: split 8 fills one wave only at 3 CTAs per SM (4 stages)
+    (8, 8192, 2048, 4, 6, 1),      # 64 tiles: split 4 either way, so the deeper ring at 2 per SM
+    (8, 4608, 3072, 8, 6, 1),      # 36 x 8 = 288 CTAs fit 2 per SM: the deeper ring
+    (16, 4096, 4096, 8, 6, 4),     # from M = 16, four reducers over few tiles
+    (32, 5120, 5120, 8, 3, 4),     # m_pad 32: 3 stages at 3 per SM keep split 8
+    (32, 4096, 14336, 8, 4, 4),    # ... 4 stages where 2 per SM keep it
+    (32, 14336, 4096, 4, 3, 1),    # 112 tiles: one reducer
+    (48, 6144, 4096, 4, 4, 4),     # m_pad 48 and 64: 4 stages, 2 per SM
+    (64, 28672, 8192, 2, 4, 1),    # 224 tiles x 2 is two waves: the last arrival reduces alone
+    (64, 1024, 512, 8, 4, 4),      # K = 512: 8 chunks, split 8
+    (64, 1024, 256, 4, 4, 4),      # K = 256: 4 chunks, no split finer than 4
+])
+def test_default_split_k_shape(M, N, K, split, stages, reducers):
+    """The measured default for split-K shapes outside the table: split K as
+    finely as one wave of CTAs at the ring's occupancy holds (at most 8, no
+    finer than K's chunks), the deeper ring where 2 CTAs per SM keep that
+    split, and four reducers per tile from M = 16 at splits of 4-8 over at
+    most 56 tiles."""
+    d = skg.skg_plan_query(M, N, K, "bf16", SMS, L2)
+    assert d["from_table"] == 0 and d["kernel"] == "splitk_tc"
+    assert (d["split_k"], d["stages"], d["reducers"], d["l2_ahead"]) == (split, stages, reducers, 2)
+
+
 def test_register_loads_when_k_is_not_a_multiple_of_256():
     d = skg.skg_plan_query(1, 5120, 5128, "bf16", SMS, L2)
     assert d["kernel"] == "gemv" and d["split_k"] == 1 and d["stages"] == 0
