@@ -225,6 +225,10 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
         kind = SKG_KERNEL_SPLITK_TC;
     } else if (M <= 2 && gemv_smem_bytes(M, K, 1, 0) > kGemvMaxSmem) {
         kind = SKG_KERNEL_SPLITK_TC;   // x does not fit the GEMV's shared memory: the split-K kernel streams it
+    } else if (M == 2 && N >= 2048 && !table_has_exact(SKG_KERNEL_GEMV, M, N, K, epi)) {
+        // measured on GB300 (9 shapes outside the table, N = 2048-28672):
+        // at two tokens the split-K kernel beats every GEMV form by 0-35%
+        kind = SKG_KERNEL_SPLITK_TC;
     }
     if (kind == SKG_KERNEL_GEMV && gemv_smem_bytes(M, K, 1, 0) > kGemvMaxSmem)
         return fail(SKG_ERR_UNSUPPORTED, "K=%d too large for the M<=2 kernel (x is staged in shared memory)", K);
@@ -238,12 +242,14 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
             d->tma_burst = row->burst;   // split 1 with bulk-copied batches: strips per copy
             d->l2_ahead = row->ahead;
             d->from_table = 1;
-        } else if (N >= 4096) {
+        } else if (N >= 1024) {
             split = 1;   // enough rows for one warp per row
             // measured: bulk-copied batches beat 16-byte loads at M = 1 and 2;
-            // at M = 1 one balanced wave beats whole rows per warp
+            // at M = 1 one balanced wave beats whole rows per warp where rows
+            // are long (K >= 5120) and not too many (N < 16384), whole rows
+            // per warp elsewhere (up to 1.4x at K <= 4096)
             if (gemv_bulk_ok(M, K, gemv_bulk_default_batch(M, K)))
-                ring = M == 1 ? 3 : 2;
+                ring = (M == 1 && K >= 5120 && N < 16384) ? 3 : 2;
             else
                 d->l2_ahead = 1;   // measured: the next 8-strip batch into L2 while this one loads
         } else {

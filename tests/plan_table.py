@@ -1,8 +1,9 @@
 """The kernel kind the picker should choose, read from the compiled-in table.
 
 M <= 2 runs the GEMV unless the measured table holds a tensor-core row for
-exactly that (M, N, K, epilogue) or x (M x K bf16) does not fit the GEMV's
-226 KB of shared memory; M > 2 always runs the tensor-core kernel.
+exactly that (M, N, K, epilogue), x (M x K bf16) does not fit the GEMV's
+226 KB of shared memory, or M = 2 with N >= 2048 and no GEMV row for exactly
+that shape; M > 2 always runs the tensor-core kernel.
 """
 from __future__ import annotations
 
@@ -25,9 +26,13 @@ def table_rows():
 
 
 _TC = {(r[1], r[2], r[3], r[4]) for r in table_rows() if r[0] == 2}
+_GEMV = {(r[1], r[2], r[3], r[4]) for r in table_rows() if r[0] == 1}
 
 
 def expected_kind(M: int, N: int, K: int, epilogue: str) -> str:
-    if M > 2 or (M, N, K, _EPI[epilogue]) in _TC or M * K * 2 > 226 * 1024:
+    key = (M, N, K, _EPI[epilogue])
+    if M > 2 or key in _TC or M * K * 2 > 226 * 1024:
+        return "splitk_tc"
+    if M == 2 and N >= 2048 and key not in _GEMV:
         return "splitk_tc"
     return "gemv"

@@ -93,20 +93,30 @@ def test_null_arguments_are_rejected():
     assert lib.skg_prefetch_l2(None, None, None) == skg.SKG_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("N,K", [(5120, 5120), (8192, 2048), (4608, 3072)])
+@pytest.mark.parametrize("N,K", [(5120, 5120), (8192, 2048), (4608, 3072), (2048, 8192), (1024, 4096),
+                                 (28672, 8192)])
 def test_default_rule_for_shapes_outside_the_table(N, K):
     """Shapes the measured table does not list fall back to the documented
-    rules: at M = 1 the one-wave bulk-copy GEMV, at M = 2 whole rows per warp
-    with bulk-copied batches (both need K % 256 == 0), and for M > 2 the
-    split-K kernel with its W tiles after the ring requested into L2 before
-    the wait for the previous kernel."""
+    rules.  At M = 1 from N = 1024 the bulk-copy GEMV: in one balanced wave
+    where rows are long (K >= 5120) and fewer than 16384, whole rows per warp
+    elsewhere (both need K % 256 == 0).  At M = 2 the split-K kernel from
+    N = 2048, below that whole rows per warp.  For M > 2 the split-K kernel
+    with its W tiles after the ring requested into L2 before the wait for the
+    previous kernel."""
     d1 = skg.skg_plan_query(1, N, K, "bf16", SMS, L2)
-    assert d1["from_table"] == 0 and d1["kernel"] == "gemv" and d1["split_k"] == 1
-    assert d1["stages"] == 3 and d1["threads"] == 256
-    assert 1 <= d1["grid"] <= 4 * SMS and d1["tile_n"] == -(-N // d1["grid"])
+    assert d1["from_table"] == 0 and d1["kernel"] == "gemv" and d1["split_k"] == 1 and d1["threads"] == 256
+    if K >= 5120 and N < 16384:
+        assert d1["stages"] == 3
+        assert 1 <= d1["grid"] <= 4 * SMS and d1["tile_n"] == -(-N // d1["grid"])
+    else:
+        assert d1["stages"] == 2 and d1["grid"] == -(-N // 8)
     d2 = skg.skg_plan_query(2, N, K, "bf16", SMS, L2)
-    assert d2["from_table"] == 0 and d2["stages"] == 2 and d2["tma_burst"] in (4, 8)
-    assert d2["grid"] == -(-N // 8)
+    assert d2["from_table"] == 0
+    if N >= 2048:
+        assert d2["kernel"] == "splitk_tc"
+    else:
+        assert d2["kernel"] == "gemv" and d2["stages"] == 2 and d2["tma_burst"] in (4, 8)
+        assert d2["grid"] == -(-N // 8)
     d8 = skg.skg_plan_query(8, N, K, "bf16", SMS, L2)
     assert d8["from_table"] == 0 and d8["kernel"] == "splitk_tc" and d8["l2_ahead"] == 2
 
@@ -140,10 +150,12 @@ def test_register_loads_when_k_is_not_a_multiple_of_256():
     assert d["kernel"] == "gemv" and d["split_k"] == 1 and d["stages"] == 0
 
 
-def test_one_wave_grid_keeps_rows_per_cta_bounded():
-    # a very tall weight: at most 256 rows per CTA, so the grid grows past one wave
-    d = skg.skg_plan_query(1, 300000, 1024, "bf16", SMS, L2)
-    assert d["stages"] == 3 and -(-300000 // d["grid"]) <= 256
+def test_tall_weights_take_whole_rows_per_warp():
+    """From N = 16384 rows (and for K < 5120) M = 1 runs whole rows per warp,
+    one row per warp, however tall the weight."""
+    for N, K in ((300000, 8192), (16384, 7168), (300000, 1024)):
+        d = skg.skg_plan_query(1, N, K, "bf16", SMS, L2)
+        assert d["kernel"] == "gemv" and d["stages"] == 2 and d["grid"] == -(-N // 8)
 
 
 def test_plan_table_rows_are_well_formed():

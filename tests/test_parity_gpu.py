@@ -351,6 +351,18 @@ def test_force_kernel_rejections_keep_the_plan():
         case.close()
 
 
+def test_forced_one_wave_grid_keeps_rows_per_cta_bounded():
+    """The one-wave GEMV form, forced on a very tall weight, takes at most 256
+    rows per CTA: its grid grows past one wave (no launch needed)."""
+    p = skg.Plan(1, 300000, 1024, "bf16")
+    try:
+        p.force(split_k=1, stages=3)
+        d = p.info()
+        assert d["stages"] == 3 and -(-300000 // d["grid"]) <= 256
+    finally:
+        p.close()
+
+
 def test_reducer_rejections_and_bounds():
     """Reducers per tile: 1, 2, 4 or 8 on a split-K plan; a GEMV plan rejects
     them; the plan reports the count a launch uses -- at most the split, and
