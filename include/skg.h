@@ -113,9 +113,10 @@ typedef struct skg_plan_desc {
     int reducers;           /* TC: the last `reducers` CTAs to finish a tile share its final
                                reduction (1, 2, 4 or 8; a launch uses fewer where the split is
                                smaller, and 1 where its grid is more than one wave); GEMV: 0 */
-    int ctas_per_sm;        /* CTAs one SM holds at once: TC, the CUDA occupancy calculator for
-                               this launch shape; GEMV, the count the plan sizes one-wave grids
-                               from.  Filled by skg_plan_info; 0 from skg_plan_query */
+    int ctas_per_sm;        /* CTAs one SM holds at once: TC, from the kernel's registers, shared
+                               memory, threads and TMEM columns at this launch shape; GEMV, the
+                               count the plan sizes one-wave grids from.  Filled by skg_plan_info;
+                               0 from skg_plan_query */
 } skg_plan_desc;
 
 typedef struct skg_plan_s *skg_plan_t;
@@ -126,10 +127,12 @@ typedef struct skg_plan_s *skg_plan_t;
  * [TS]: M <= 2 -> SKG_KERNEL_GEMV, M > 2 -> SKG_KERNEL_SPLITK_TC, except that
  * an M <= 2 shape runs the tensor-core kernel where the table of measured
  * timings holds a tensor-core row for exactly that (M,N,K,epilogue) (written
- * only where it was faster on GB300), or where K is too long for the GEMV
- * to stage x in shared memory (M = 1: K > 115,200); inside each kind the split
- * and pipeline depth come from that table (nearest M for a listed
- * (N,K,epilogue)), else from an occupancy rule.
+ * only where it was faster on GB300), where K is too long for the GEMV to
+ * stage x in shared memory (M = 1: K > 115,200), or at M = 2 from N = 2048
+ * unless the table holds a GEMV row for exactly that shape; inside each kind
+ * the split and pipeline depth come from that table (nearest M for a listed
+ * (N,K,epilogue)), else from a rule measured on GB300 (split-K: the finest
+ * split, at most 8, whose grid is one wave at the ring's occupancy).
  * Constraints: 1 <= M <= 64, N >= 1, K >= 8 and K % 8 == 0, epilogue valid.
  * Errors: SKG_ERR_INVALID_ARG (sizes, enum, NULL out), SKG_ERR_UNSUPPORTED.
  */
