@@ -656,6 +656,45 @@ def measure_config(name, dev, s, torch_stream, args, peak_hbm, peak_tf, l2_bytes
         wl.close()
 
 
+def chain_graph(wl, torch_stream, steps, side_frac=None):
+    """The chain's whole step captured once as a CUDA graph (programmatic
+    edges between its launches) and replayed; with side_frac, each next
+    weight's skg_prefetch_l2 runs on a forked side-stream branch of the graph,
+    joined before the next projection."""
+    import torch
+    from projection_gemm_gb300 import skg
+    dev = torch_stream.device
+    cap, side = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    wl.bind_streams([cap, side])
+    kw = {}
+    if side_frac is not None:
+        for o in wl.ops:
+            skg.skg_plan_set_prefetch_fraction(o["plan"].handle, side_frac)
+        kw = {"side": (side, side.cuda_stream), "side_join": True}
+    cap.wait_stream(torch_stream)
+    with torch.cuda.stream(cap):
+        wl.step(cap.cuda_stream, **kw)        # descriptors and attributes outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        wl.step(cap.cuda_stream, **kw)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    main = torch.cuda.current_stream(dev)      # replay() launches on the current stream
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(main)
+    for _ in range(steps):
+        g.replay()
+    b.record(main)
+    torch.cuda.synchronize()
+    el = a.elapsed_time(b) / 1e3
+    del g
+    wl.bind_streams([torch_stream])
+    return {"us_per_step": round(el / steps * 1e6, 3), "gbs": round(wl.weight_bytes() * steps / el / 1e9, 1)}
+
+
 def chain_variants(wl, s, torch_stream, steps, l2_bytes):
     """The chain end to end per M and in total, without prefetch, with the
     in-launch prefetch of the next weight, and with skg_prefetch_l2 of the
@@ -712,6 +751,8 @@ def chain_variants(wl, s, torch_stream, steps, l2_bytes):
     ])
     set_next(0.0)
     wl.bind_streams([torch_stream])
+    out["captured_graph"] = chain_graph(wl, torch_stream, steps)
+    out["captured_graph_side_stream_50pct_l2"] = chain_graph(wl, torch_stream, steps, side_frac=0.5)
     out["group_launch_per_m_ordered"] = chain_groups(wl, s, torch_stream, steps)
     out["router_and_latent_as_one_launch"] = chain_router_latent(wl, s, torch_stream, steps)
     return out
