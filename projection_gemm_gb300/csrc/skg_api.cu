@@ -184,6 +184,15 @@ bool table_has_exact(int kind, int M, int N, int K, int epi)
     return false;
 }
 
+// Reducers per tile where neither the table nor the caller sets them,
+// measured on GB300: from M = 16 four reducers beat one wherever a tile's
+// split is 4 or 8 and the tiles are few (<= 56); with more tiles, or
+// shorter splits, the waits cost more than the shorter reduction saves.
+int default_reducers(int M, int split, int n_tiles)
+{
+    return (M >= 16 && split >= 4 && n_tiles <= 56) ? 4 : 1;
+}
+
 // force_kind 0: the picker chooses the kernel kind.
 skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg_plan_desc *d,
                  int force_kind = 0)
@@ -300,11 +309,7 @@ skg_status query(int M, int N, int K, int epi, int num_sms, size_t l2_bytes, skg
             stages = mp == 16 ? (deep ? 6 : 4) : (mp == 32 ? (deep ? 4 : 3) : 4);
             d->l2_ahead = 2;   // measured: 2 tiles after the ring into L2 before the wait
         }
-        // Reducers per tile: the row's, else the measured default -- from
-        // M = 16 four reducers beat one wherever a tile's split is 4 or 8 and
-        // the tiles are few (<= 56); with more tiles, or shorter splits, the
-        // waits cost more than the shorter reduction saves.
-        d->reducers = (row && row->reducers > 0) ? row->reducers : ((M >= 16 && split >= 4 && n_tiles <= 56) ? 4 : 1);
+        d->reducers = (row && row->reducers > 0) ? row->reducers : default_reducers(M, split, n_tiles);
         fill_tc(d, split, stages, burst);
     }
     return SKG_OK;
@@ -488,6 +493,7 @@ struct skg_plan_s {
     size_t ws_cap = 0;
     std::vector<void *> retired;      // outgrown workspaces: a captured graph may still use them
     int want_reducers = 0;            // requested reducers per tile (table, default or skg_plan_set_reducers)
+    bool reducers_set = false;        // want_reducers came from skg_plan_set_reducers
     int occ_m_pad = 0, occ_stages = 0; // shape of the split-K launch tc_ctas_per_sm was measured for
     int tc_ctas_per_sm = 1;
     const void *next_w = nullptr;     // prefetched into L2 by this plan's launches
@@ -729,6 +735,8 @@ skg_status skg_plan_force(skg_plan_t p, int split_k, int stages, int grid, int t
     }
     d.from_table = 0;
     p->d = d;
+    if (!p->reducers_set && d.kernel_kind == SKG_KERNEL_SPLITK_TC)
+        p->want_reducers = default_reducers(d.M, d.split_k, (d.N + kTileN - 1) / kTileN);   // the forced shape's default
     p->wmaps.clear();
     p->xmaps.clear();
     return finish_update(p);
@@ -760,6 +768,7 @@ skg_status skg_plan_force_kernel(skg_plan_t p, int kind)
         fill_tc(&d, kChunks / p->k_ranks, d.stages, d.tma_burst);
     p->d = d;
     p->want_reducers = d.reducers;   // re-planned: the new shape's default
+    p->reducers_set = false;
     p->wmaps.clear();
     p->xmaps.clear();
     return finish_update(p);
@@ -791,8 +800,10 @@ skg_status skg_plan_set_k_shard(skg_plan_t p, int rank, int ranks)
     if (d.kernel_kind == SKG_KERNEL_SPLITK_TC && d.split_k > kChunks / ranks)
         fill_tc(&d, kChunks / ranks, d.stages, d.tma_burst);   // a rank's CTAs split its chunks
     p->d = d;
-    if (replan)
+    if (replan) {
         p->want_reducers = d.reducers;
+        p->reducers_set = false;
+    }
     p->k_rank = rank;
     p->k_ranks = ranks;
     refresh_prefetch_bytes(p);
@@ -864,6 +875,7 @@ skg_status skg_plan_set_reducers(skg_plan_t p, int reducers)
     if (p->d.kernel_kind != SKG_KERNEL_SPLITK_TC)
         return fail(SKG_ERR_UNSUPPORTED, "reducers apply to the split-K kernel only");
     p->want_reducers = reducers;
+    p->reducers_set = true;
     return finish_update(p);
 }
 

@@ -379,7 +379,11 @@ def test_reducer_rejections_and_bounds():
             gemv.set_reducers(2)
         assert e.value.status == skg.SKG_ERR_UNSUPPORTED
         sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert tc.info()["reducers"] == 4                       # the default at M = 64, split 4, 56 tiles
+        tc.force(split_k=2)
+        assert tc.info()["reducers"] == 1                       # a forced split takes its own default
         tc.force(split_k=4)
+        assert tc.info()["reducers"] == 4
         tc.set_reducers(8)
         assert tc.info()["reducers"] == 4                       # at most the split
         tc.force(split_k=16)
