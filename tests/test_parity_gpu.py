@@ -72,6 +72,10 @@ SMALL = [
     (16, 1024, 1024, "bf16_residual"), (17, 640, 2056, "bf16"), (33, 300, 200, "bf16"),
     (48, 1000, 1048, "fp32"), (63, 129, 72, "bf16_residual"), (64, 1000, 1048, "bf16"),
     (64, 128, 8, "bf16"), (4, 1, 64, "bf16"), (32, 2000, 3080, "bf16_residual"),
+    # M = 2 at the kind boundary of the default rule: the split-K kernel from N = 2048, the GEMV below
+    (2, 2048, 1024, "bf16_residual"), (2, 2047, 1000, "bf16"), (2, 3000, 264, "fp32"),
+    # the default rule's deeper ring and its one-wave split at m_pad 32 and 48
+    (32, 4100, 2048, "bf16"), (48, 1030, 4096, "bf16_residual"),
 ]
 
 
