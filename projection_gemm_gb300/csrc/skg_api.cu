@@ -510,7 +510,7 @@ struct skg_plan_s {
 struct skg_group_s {
     int n = 0, M = 0, m_pad = 0, device = 0, num_sms = 0, stages = 0, grid = 0, units = 0;
     int N[kGroupMax] = {}, K[kGroupMax] = {}, epi[kGroupMax] = {}, dep[kGroupMax] = {};
-    int split[kGroupMax] = {}, n_tiles[kGroupMax] = {}, ahead[kGroupMax] = {};
+    int split[kGroupMax] = {}, n_tiles[kGroupMax] = {}, ahead[kGroupMax] = {}, reducers[kGroupMax] = {};
     size_t ws_off[kGroupMax] = {}, ctr_off[kGroupMax] = {}, done_off = 0, ws_bytes = 0;
     void *ws = nullptr;               // partials and counters of every projection, then done[]
     unsigned int *err_host = nullptr; // mapped pinned word
@@ -1104,6 +1104,7 @@ skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilog
         // the picker's split for this projection, at most 8 (any split gives the same bits)
         g->split[i] = std::min(8, d.split_k);
         g->ahead[i] = d.l2_ahead;
+        g->reducers[i] = std::min(d.reducers, g->split[i]);
         g->n_tiles[i] = (N[i] + kTileN - 1) / kTileN;
         g->ws_off[i] = off;
         off += (tc_partial_bytes(M, N[i], g->split[i]) + 255) / 256 * 256;
@@ -1133,6 +1134,16 @@ skg_status skg_group(int n, int M, const int *N, const int *K, const int *epilog
     // one wave: CTAs beyond the SMs' capacity would only start once others
     // finished (correct -- units are handed out in order -- but idle)
     g->grid = std::min(g->units, per_sm * sms);
+    // Reducers per tile beyond the last arrival wait for the tile's other
+    // units: allowed only where every CTA owns exactly one unit (no
+    // dependencies, so CTA c runs unit c, and the grid holds every unit in
+    // one wave), as in the one-projection kernel.
+    bool has_dep = false;
+    for (int i = 1; i < n; ++i)
+        has_dep = has_dep || g->dep[i];
+    if (has_dep || g->units > g->grid)
+        for (int i = 0; i < n; ++i)
+            g->reducers[i] = 1;
     e = cudaMalloc(&g->ws, g->ws_bytes);
     if (e == cudaSuccess)
         e = cudaMemset(g->ws, 0, g->ws_bytes);
@@ -1215,6 +1226,7 @@ skg_status skg_group_run(skg_group_t g, const void *const *x, const void *const 
         P.epilogue = g->epi[i];
         P.dep = g->dep[i];
         P.ahead = g->ahead[i];
+        P.reducers = std::max(1, g->reducers[i]);
         P.unit_begin = unit;
         unit += g->n_tiles[i] * g->split[i];
     }

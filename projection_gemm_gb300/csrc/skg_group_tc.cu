@@ -119,12 +119,12 @@ __device__ __forceinline__ Unit unit_of(const GroupParams &g, int u)
 // 4 loads in flight per thread (the unit loop keeps more registers live;
 // 8 or 16, as there, measured slower here).
 template <int MPAD>
-__device__ __forceinline__ void group_reduce(const GroupProj *P, int tile, int sp, int et)
+__device__ __forceinline__ void group_reduce(const GroupProj *P, int tile, int sp, int et, int i0, int i1)
 {
     switch (P->split) {
-    case 2: reduce_tile_v4<2, 4>(*P, tile, sp, et); break;
-    case 4: reduce_tile_v4<4, 4>(*P, tile, sp, et); break;
-    default: reduce_tile_v4<8, 4>(*P, tile, sp, et); break;
+    case 2: reduce_tile_v4<2, 4>(*P, tile, sp, et, i0, i1); break;
+    case 4: reduce_tile_v4<4, 4>(*P, tile, sp, et, i0, i1); break;
+    default: reduce_tile_v4<8, 4>(*P, tile, sp, et, i0, i1); break;
     }
 }
 
@@ -458,14 +458,33 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
                         P.ws[((static_cast<size_t>(U.split) * P.n_tiles + U.tile) * P.M + m) * kTileN + row] = cur[c];
                 }
             }
-            // Arrive on the tile's counter (see the one-projection kernel).
+            // Arrive on the tile's counter (see the one-projection kernel):
+            // the last R arrivals share the tile's reduction.  R > 1 only
+            // when every CTA owns one unit and nothing depends on anything,
+            // so a waiter waits only for CTAs that run their one unit to its
+            // arrival without waiting.
             epi_bar_sync();
+            const int R = P.reducers;
             if (ew == 0 && lane == 0) {
-                const unsigned old = atom_add_acq_rel_gpu(&P.counters[U.tile], 1u);
-                flags[1] = (old == static_cast<unsigned>(P.split - 1)) ? 1 : 0;
+                const int old = static_cast<int>(atom_add_acq_rel_gpu(&P.counters[U.tile], 1u) & 0xFFFFu);
+                const int first = P.split - R;
+                int role = 0;
+                if (old >= first) {
+                    if (old == P.split - 1 ||
+                        wait_counter(&P.counters[U.tile], static_cast<unsigned>(P.split), g.timeout_ns, &flags[0]))
+                        role = old - first + 1;
+                    else
+                        group_failure(g, &flags[0], kErrTimeoutEpilogue);
+                }
+                // the last reducer to see every arrival returns the counter to zero
+                if (role && R > 1 &&
+                    (atom_add_acq_rel_gpu(&P.counters[U.tile], 1u << 16) >> 16) == static_cast<unsigned>(R - 1))
+                    P.counters[U.tile] = 0;
+                flags[1] = role;
             }
             epi_bar_sync();
             if (flags[1]) {
+                const int role = flags[1];
                 const int L = kChunks / P.split;
                 const int sp = (chunks_present(P.nkb) + L - 1) / L;  // splits holding a value
                 if (P.dep && U.j > 0 && P.res) {
@@ -478,11 +497,17 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
                         break;
                 }
                 // splits are 2, 4 or 8 here (the group caps them; any split
-                // gives the same bits)
-                group_reduce<MPAD>(&P, U.tile, sp, threadIdx.x - 64);
-                // every y store of the tile comes before the release of done[j]
+                // gives the same bits); share r of R: whole columns
+                // [r * ceil(M / R), (r + 1) * ceil(M / R))
+                const int items = P.M * (kTileN / 4);
+                const int share = (P.M + R - 1) / R * (kTileN / 4);
+                group_reduce<MPAD>(&P, U.tile, sp, threadIdx.x - 64, min(items, (role - 1) * share),
+                                   min(items, role * share));
+                // every y store of the tile comes before the release of
+                // done[j] (with one reducer; R > 1 only without dependencies,
+                // where nothing reads done[j])
                 epi_bar_sync();
-                if (ew == 0 && lane == 0) {
+                if (ew == 0 && lane == 0 && R == 1) {
                     P.counters[U.tile] = 0;
                     red_release_gpu_add(&g.done[U.j], 1u);
                 }

@@ -94,6 +94,8 @@ struct GroupProj {              // aligned as CUtensorMap
     int dep;                // 1: x read only after the previous projection of the group is complete
     int ahead;              // W k-blocks past the ring prefetched to L2 before a wait for x
     int unit_begin;         // first work unit (tile, split) of this projection
+    int reducers;           // R: the last R arrivals of a tile each reduce 1/R of it (R > 1 only when every
+                            // CTA owns one unit and the group has no dependencies)
 };
 
 constexpr int kGroupDoneExit = kGroupMax;

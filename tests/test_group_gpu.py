@@ -88,8 +88,14 @@ def test_decode_layer_group_matches_skg_run(M):
     (17, [(200, 300, "bf16"), (1024, 1024, "bf16_residual")]),
     (64, [(8, 128, "bf16"), (7168, 384, "fp32"), (520, 4096, "bf16_residual"), (1048, 1, "bf16")]),
     (48, [(4096, 7168, "bf16_residual")]),
+    # the router and latent projections: one unit per CTA, several reducers per tile
+    (64, [(7168, 384, "fp32"), (7168, 4096, "bf16")]),
+    (16, [(7168, 384, "fp32"), (7168, 4096, "bf16")]),
 ])
 def test_ragged_groups_without_dependencies(M, shapes):
+    """Groups without dependencies: every output equals skg_run's and meets
+    the oracle; where the grid holds every unit, the last arrivals of a tile
+    share its reduction (the bits do not depend on how many share it)."""
     _group_case(M, shapes, dep=None, seed=400 + M, runs=2)
 
 
