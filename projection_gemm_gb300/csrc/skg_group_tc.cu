@@ -177,15 +177,21 @@ __global__ void __launch_bounds__(kTcThreads, (MPAD <= 32) ? 3 : 2) splitk_group
         flags[1] = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, Sh::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
+    // As in the one-projection kernel: the producer starts once the
+    // barriers exist, the MMA and epilogue warps once TMEM is allocated.
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
     pdl_launch_dependents();
+    uint32_t tmem_base = 0;
+    if (warp != 0) {
+        if (warp == 1) {
+            tmem_alloc(tmem_slot, Sh::kTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        asm volatile("bar.sync 2, 288;" ::: "memory");   // warps 1..9
+        tc_fence_after();
+        tmem_base = *tmem_slot;
+    }
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer

@@ -126,15 +126,24 @@ splitk_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         flags[1] = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, Sh::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
+    // The producer starts as soon as the barriers exist; the MMA and
+    // epilogue warps meet again (named barrier 2) once warp 1 has allocated
+    // TMEM.  A CTA that starts late, as the previous kernel's CTAs leave,
+    // so requests its first weight tiles without waiting for the allocation
+    // (measured on GB300: the batch sweep's step 136.4 -> 134.0 us).
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
     pdl_launch_dependents();
+    uint32_t tmem_base = 0;
+    if (warp != 0) {
+        if (warp == 1) {
+            tmem_alloc(tmem_slot, Sh::kTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        asm volatile("bar.sync 2, 288;" ::: "memory");   // warps 1..9
+        tc_fence_after();
+        tmem_base = *tmem_slot;
+    }
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
